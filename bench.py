@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A8 skinny linear on GB300: the 27B-class decode step.
+
+One step = the 257 decode linears of a 27B-class decoder, in order: 64 layers
+of (QKV 5120->7168, O 5120->5120, gate+up 5120->34816, down 17408->5120) and
+the LM head 5120->152064, each one launch of the fused bf16 -> int8 -> W4A8
+GEMV entry point (woq_w4a8_linear_bf16), captured once in a CUDA graph.
+Weights are distinct synthetic tensors per linear (11.3 GB packed, far larger
+than the 129 MB L2, so every step streams them from HBM); activations are
+seeded bf16 N(0,1) with 1 % x20 outlier channels (synthetic.py).
+
+Prints one JSON line (rank 0).  `value` is the achieved algorithmic HBM
+bandwidth of the step in GB/s (packed int4 weights + fp16 group scales +
+bf16 activations read once), summed over ranks; ms_per_step and the M = 3 / 4
+step times ride along.  `--impl reference` times the CPU oracle instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A8 skinny-GEMV HBM GB/s & % of GB300 peak at M=1,3; µs per 27B-class step"
+WORKLOAD = ("27B-class decode step, W4A8: 64 x (QKV 5120->7168, O 5120->5120, gate+up 5120->34816, "
+            "down 17408->5120) + LM head 5120->152064 = 257 linears")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--m", type=int, default=1, help="activation rows of the headline step")
+    ap.add_argument("--extra-m", default="3,4", help="also time the step at these M (comma list, '' for none)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-div", type=int, default=8, help="oracle sample: 1/div of every linear's rows")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def algorithmic_bytes(linears, M, bits=4):
+    """Packed weights + fp16 group scales + bf16 activations read once, per step."""
+    tot = 0
+    for _, K, N in linears:
+        tot += N * K * bits // 8 + 2 * N * (K // 128) + 2 * M * K
+    return tot
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """Per-step DRAM bytes of the GEMV kernel from the committed ncu summary (None if absent)."""
+    p = os.path.join(ROOT, "profiles", "gemv_w4a8_27b_step_m1.md")
+    try:
+        with open(p) as f:
+            for line in f:
+                if line.startswith("dram_bytes_per_step:"):
+                    return int(line.split(":")[1].strip())
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self, util_floor_mhz=0):
+        sms, maxes, reasons, powers = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, mx, pw = float(f[1]), float(f[2]), float(f[3])
+            except ValueError:
+                continue
+            powers.append(pw)
+            sms.append(sm)
+            maxes.append(mx)
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        # samples taken while the GPU was busy: the top half by power draw
+        pw_cut = statistics.median(powers)
+        loaded = [s for s, p in zip(sms, powers) if p >= pw_cut] or sms
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms), "power_w_max": max(powers)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Step:
+    """The 27B-class decode step on one GPU: weights packed in HBM, one CUDA graph per M."""
+
+    def __init__(self, device, seed=2, cpu_sample_div=0):
+        import torch
+
+        import synthetic
+        import weight_only_quantised_gb300 as woq
+        self.torch, self.woq, self.synthetic = torch, woq, synthetic
+        self.device = device
+        self.linears = synthetic.step_27b()
+        self.packed = []
+        self.cpu_sample = []  # (K, N rows, canonical w rows, scale rows) for the oracle baseline
+        for name, K, N in self.linears:
+            w, s = synthetic.weights(4, N, K, synthetic.sub_seed(seed, name), device=device)
+            p = torch.empty(woq.woq_packed_bytes(4, N, K), dtype=torch.uint8, device=device)
+            woq.woq_pack_device(4, w, s.view(torch.int16), N, K, p)
+            self.packed.append(p)
+            if cpu_sample_div:
+                rows = max(1, N // cpu_sample_div)
+                self.cpu_sample.append((K, rows, w[:rows].cpu().numpy(),
+                                        synthetic.to_numpy_u16(s[:rows])))
+            del w, s
+        torch.cuda.synchronize()
+        self.graphs = {}
+
+    def buffers(self, M, seed=2):
+        torch, synthetic, woq = self.torch, self.synthetic, self.woq
+        xs = {K: synthetic.activations(M, K, synthetic.sub_seed(seed, "x", M, K), outliers=True,
+                                       device=self.device) for K in sorted({K for _, K, _ in self.linears})}
+        ys = {N: torch.empty((M, N), dtype=torch.float32, device=self.device)
+              for N in sorted({N for _, _, N in self.linears})}
+        wsb = max(woq.woq_workspace_bytes(4, M, N, K) for _, K, N in self.linears)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
+        return xs, ys, ws
+
+    def launch_all(self, xs, ys, ws):
+        woq = self.woq
+        for (name, K, N), p in zip(self.linears, self.packed):
+            woq.woq_w4a8_linear_bf16(p, xs[K], N, K, ys[N], ws)
+
+    def capture(self, M):
+        torch = self.torch
+        xs, ys, ws = self.buffers(M)
+        stream = torch.cuda.Stream(device=self.device)
+        with torch.cuda.stream(stream):
+            self.launch_all(xs, ys, ws)  # warm-up outside the capture (sets kernel attributes)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.launch_all(xs, ys, ws)
+        torch.cuda.synchronize()
+        assert self.woq.woq_read_status(ws) == 0
+        self.graphs[M] = (g, xs, ys, ws)
+        return self.graphs[M]
+
+    def time_device(self, M, steps, warmup, barrier, sampler_gpu=None):
+        torch = self.torch
+        g, xs, ys, ws = self.graphs.get(M) or self.capture(M)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        clocks = None
+        barrier()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(sampler_gpu) if sampler_gpu is not None else None
+        if sampler:
+            sampler.__enter__()
+        start.record()
+        for _ in range(steps):
+            g.replay()
+        end.record()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.__exit__(None, None, None)
+            clocks = sampler.summary()
+        barrier()
+        assert self.woq.woq_read_status(ws) == 0
+        return start.elapsed_time(end), clocks
+
+    def time_e2e(self, M, steps, warmup):
+        """Per step: pinned host -> device copy of the step's activations, the graph, and a
+        device -> pinned host read of the LM-head output; synchronised every step."""
+        torch = self.torch
+        g, xs, ys, ws = self.graphs.get(M) or self.capture(M)
+        xh = {K: x.cpu().pin_memory() for K, x in xs.items()}
+        n_out = self.linears[-1][2]
+        yh = torch.empty((M, n_out), dtype=torch.float32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in xh.values())
+        d2h = yh.numel() * yh.element_size()
+
+        def one():
+            for K, x in xs.items():
+                x.copy_(xh[K], non_blocking=True)
+            g.replay()
+            yh.copy_(ys[n_out], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(warmup):
+            one()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        dt = (time.perf_counter() - t0) / steps
+        return dt, h2d, d2h
+
+
+def cpu_baseline_oracle(sample, M, seed=2):
+    """The oracle (single thread, as it stands) on 1/div of every linear's rows, M activation rows."""
+    import oracle
+    import synthetic
+    xs = {}
+    total_bytes = 0
+    t0 = time.perf_counter()
+    for K, rows, wn, sn in sample:
+        if K not in xs:
+            xs[K] = synthetic.to_numpy_u16(synthetic.activations(M, K, synthetic.sub_seed(seed, "x", M, K)))
+        oracle.linear_bf16(4, wn, sn, rows, K, xs[K])
+        total_bytes += rows * K // 2 + 2 * rows * (K // 128) + 2 * M * K
+    dt = time.perf_counter() - t0
+    return total_bytes / dt / 1e9, dt, total_bytes
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    step = Step(device, cpu_sample_div=args.cpu_sample_div if do_cpu else 0)
+    M = args.m
+    bytes_step = algorithmic_bytes(step.linears, M)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    gpu_index = vis.split(",")[local].strip() if vis else str(local)
+
+    ms_total, clocks = step.time_device(M, args.steps, args.warmup, barrier, sampler_gpu=gpu_index)
+    ms_total = max_over_ranks(ms_total)
+    ms_step = ms_total / args.steps
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+
+    extra = {}
+    for em in [int(v) for v in args.extra_m.split(",") if v.strip()]:
+        if em == M:
+            continue
+        k = min(args.steps, 300)
+        ms_e, _ = step.time_device(em, k, min(args.warmup, 5), barrier)
+        ms_e = max_over_ranks(ms_e) / k
+        b_e = algorithmic_bytes(step.linears, em)
+        extra[f"m{em}"] = {"ms_per_step": round(ms_e, 4), "us_per_step": round(ms_e * 1e3, 1),
+                           "gbs": round(b_e / (ms_e * 1e-3) / 1e9, 1),
+                           "vs_m1_time": round(ms_e / ms_step, 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        k = min(args.steps, 200)
+        dt, h2d, d2h = step.time_e2e(M, k, min(args.warmup, 5))
+        dt = max_over_ranks(dt)
+        e2e = {"value": round(world * bytes_step / dt / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 4)}
+
+    cpu = None
+    if do_cpu:
+        v, dt, nbytes = cpu_baseline_oracle(step.cpu_sample, M)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first 1/{args.cpu_sample_div} of the rows of all 257 linears of the step, M={M} "
+                         f"({nbytes / 1e9:.2f} GB of weights+scales, {dt:.1f} s, single thread)"}
+
+    peak, peak_kind = measured_peak()
+    achieved = bytes_step / (ms_step * 1e-3) / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "us_per_step": round(ms_step * 1e3, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "s8xs4->s32, f32 scale",
+        "data": "synthetic (seeded; random weights of the 27B-class shapes)",
+        "config": {"workload": WORKLOAD, "m": M, "linears": len(step.linears),
+                   "bytes_per_step": bytes_step, "entry": "woq_w4a8_linear_bf16 (fused bf16 quant + GEMV)",
+                   "cuda_graph": True, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: 11.3 GB of distinct weights streamed per step"},
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": peak_kind, "kernel": "woq::kern::gemv_kernel<4, M, fused>",
+                     "per": "step (257 launches)"},
+        "extra_m": extra,
+        "e2e": e2e,
+        "gpu_launches": len(step.linears) * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle on the host cores: each step is a bounded row sample of one of the
+    step's linears (cycling through all 257), sized so the whole run takes about a minute."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import synthetic
+    linears = synthetic.step_27b()
+    M = args.m
+    # calibrate the oracle's rate on this host
+    K0, N0 = 5120, 64
+    w, s = synthetic.weights(4, N0, K0, 0)
+    x = synthetic.to_numpy_u16(synthetic.activations(M, K0, 0))
+    t0 = time.perf_counter()
+    oracle.linear_bf16(4, w.numpy(), synthetic.to_numpy_u16(s), N0, K0, x)
+    rate = N0 * K0 / max(time.perf_counter() - t0, 1e-6)  # weights per second
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    cache = {}
+    total_b, total_t = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        name, K, N = linears[i % len(linears)]
+        rows = int(min(N, max(1, budget * rate / K)))
+        key = (name, rows)
+        if key not in cache:
+            wt, st = synthetic.weights(4, rows, K, synthetic.sub_seed(2, name, rows))
+            xk = synthetic.to_numpy_u16(synthetic.activations(M, K, synthetic.sub_seed(2, "x", M, K)))
+            cache = {key: (wt.numpy(), synthetic.to_numpy_u16(st), xk)}
+        wn, sn, xk = cache[key]
+        t0 = time.perf_counter()
+        oracle.linear_bf16(4, wn, sn, rows, K, xk)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            total_t += dt
+            total_b += rows * K // 2 + 2 * rows * (K // 128) + 2 * M * K
+    value = total_b / total_t / 1e9
+    ms_step = total_t / args.steps * 1e3
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int64 dots, f32 terms, f64 sum",
+        "data": "synthetic (seeded; random weights of the 27B-class shapes)",
+        "config": {"workload": WORKLOAD, "m": M, "linears": len(linears),
+                   "sample": "each step: a row sample of one linear of the step, cycling through all 257"},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(value, 4), "unit": "GB/s",
+                         "sample": f"{args.steps} steps of row samples (~{budget:.2f} s each), single thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

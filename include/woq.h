@@ -1,0 +1,198 @@
+/*
+ * woq.h - C ABI of the weight-only-quantised skinny linear for NVIDIA GB300 (sm_103a).
+ *
+ * The op ("Doubling LLM token rates in ComfyUI", blog.comfy.org, sections
+ * "What is the bottleneck?" and "Optimizing the Linear Kernel"):
+ *
+ *     y[M x N] = dequant(W[N x K]) . quant8(x[M x K]),   M = 1 .. 4
+ *
+ * W holds 4-bit (W4A8) or 6-bit (W6A8) signed weights with one fp16 scale per
+ * row and group of 128 consecutive k; x is quantised per row to int8 with
+ * scale amax/127 (round half to even); per group the int8 x int4/int6 dot
+ * product is exact in int32, then scaled: term = (d * wscale) * ascale, and
+ * y = sum of the terms over the groups (fp32).
+ *
+ * Conventions for every entry point
+ *   - Return value: a woq_status (0 = WOQ_OK).  Arguments are validated on the
+ *     host before anything is launched; an invalid call launches nothing and
+ *     changes no buffer.  Nothing aborts, traps or waits without a bound.
+ *   - "host" pointers are ordinary CPU memory; "device" pointers are CUDA
+ *     global memory of the current device.  The caller owns every buffer; the
+ *     library allocates no memory (device or pinned) in any entry point.
+ *   - Device entry points are asynchronous on the given stream (NULL = the
+ *     legacy default stream).  Launch failures return WOQ_ERR_CUDA; a fault in
+ *     a kernel surfaces at the caller's next synchronisation.
+ *   - Device buffers must be 16-byte aligned, except y, ascale and dots (4 bytes).
+ *   - Empty shapes are valid: M == 0 or N == 0 launches nothing and returns
+ *     WOQ_OK; K == 0 (no groups) zero-fills y.
+ *   - Weights use the packed device layout written by woq_pack_w4 /
+ *     woq_pack_w6 (or their device twins).  Its 256-byte header records
+ *     (bits, N, K); kernels check it and, on a mismatch, set a flag in the
+ *     workspace status word and leave y untouched.
+ *   - Kernels are launched with programmatic dependent launch: a woq kernel may
+ *     start streaming weights while the previous kernel in the stream is still
+ *     running, and waits for it before it reads activations or touches y or the
+ *     workspace.  Weights must therefore not be written by the kernel that
+ *     directly precedes a woq launch in the stream if that kernel is itself a
+ *     woq GEMV/linear launch (woq kernels never write weights).
+ */
+#ifndef WOQ_H
+#define WOQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define WOQ_API __attribute__((visibility("default")))
+#else
+#define WOQ_API
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* woq_stream_t;
+
+typedef enum {
+  WOQ_OK = 0,
+  WOQ_ERR_NULL = 1,      /* a required pointer is NULL */
+  WOQ_ERR_ALIGN = 2,     /* a device pointer is not 16-byte aligned */
+  WOQ_ERR_SHAPE = 3,     /* M, N, K or bits outside the supported range */
+  WOQ_ERR_WORKSPACE = 4, /* workspace smaller than woq_workspace_bytes() */
+  WOQ_ERR_LAYOUT = 5,    /* packed buffer size or header does not match (bits, N, K) */
+  WOQ_ERR_CUDA = 6,      /* a CUDA runtime call failed (launch, copy, attribute query) */
+  WOQ_ERR_DEVICE = 7     /* a kernel reported an error in the workspace status word */
+} woq_status;
+
+/* Bits of the workspace status word (see woq_read_status). */
+#define WOQ_DEVERR_HEADER 0x1u  /* packed header did not match the call's (bits, N, K) */
+#define WOQ_DEVERR_TIMEOUT 0x2u /* a bounded pipeline wait ran out (the kernel gave up) */
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+WOQ_API int woq_version(void);
+
+/* Human-readable name of a status code. Never NULL. */
+WOQ_API const char* woq_status_string(int status);
+
+/* Largest supported M (activation rows). */
+WOQ_API int woq_max_m(void);
+
+/* ---------------------------------------------------------------------------
+ * Packing (section "Optimizing the Linear Kernel": weights and their
+ * per-group scales are interleaved in the order the kernel consumes them, so
+ * each thread block streams one contiguous run).
+ *
+ * Canonical (checkpoint) layout, the input of the packers:
+ *   int4: q4 uint8 [N][K/2]; weight (n, k) is the low nibble of byte k/2 when k
+ *         is even and the high nibble when k is odd; two's complement [-8, 7].
+ *   int6: q6 uint8 [N][3K/4]; weights 4j .. 4j+3 of a row are the four 6-bit
+ *         fields (value i in bits 6i .. 6i+5) of the little-endian 24-bit word
+ *         in bytes 3j .. 3j+2; two's complement [-32, 31].
+ *   scales: uint16 [N][K/128], fp16 bit patterns, scale of row n, group g.
+ * Requirements: N >= 0, K >= 0, K % 128 == 0.
+ * Packed layout: a 256-byte header followed by ceil(N/128) * (K/128) blocks, one
+ * per (128-row tile, 128-k group), tile-major; each block holds the tile's 128
+ * group scales followed by its weights in the order one consumer warp reads
+ * them.  Rows beyond N are zero.  The size is woq_packed_bytes(bits, N, K).
+ * --------------------------------------------------------------------------- */
+
+/* Bytes of the packed layout for (bits, N, K); 0 if the shape is invalid. */
+WOQ_API size_t woq_packed_bytes(int bits, int N, int K);
+
+/* Host -> host.  dst must hold woq_packed_bytes(4, N, K) bytes. Synchronous. */
+WOQ_API int woq_pack_w4(const uint8_t* q4, const uint16_t* scales_f16, int N, int K, void* dst, size_t dst_bytes);
+
+/* Host -> host.  dst must hold woq_packed_bytes(6, N, K) bytes. Synchronous. */
+WOQ_API int woq_pack_w6(const uint8_t* q6, const uint16_t* scales_f16, int N, int K, void* dst, size_t dst_bytes);
+
+/* Host -> host inverse of the packers: packed bytes back to the canonical layout
+ * (q: N * row bytes, scales: N * K/128).  Checks the header. Synchronous. */
+WOQ_API int woq_unpack(int bits, const void* packed, size_t packed_bytes, int N, int K, uint8_t* q, uint16_t* scales_f16);
+
+/* Device -> device twin of woq_pack_w4 / woq_pack_w6 (bits = 4 or 6): the
+ * canonical weights and scales already sit in device memory; dst is a separate
+ * device buffer of woq_packed_bytes(bits, N, K) bytes.  Produces the same bytes
+ * as the host packer.  Asynchronous on the stream. */
+WOQ_API int woq_pack_device(int bits, const uint8_t* q_dev, const uint16_t* scales_dev, int N, int K, void* dst_dev,
+                    size_t dst_bytes, woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Workspace.  GEMV / linear launches split the weight stream evenly over the
+ * GPU's SMs; a 128-row tile that straddles two CTAs is finished by the last
+ * CTA to reach it, through partial sums and a ticket counter in the workspace.
+ * The workspace (device, caller-owned) must be zero-filled once before first
+ * use (woq_workspace_init); every launch leaves its counters at zero again.
+ * One workspace must not be used by two launches that can run at the same time.
+ * Its size depends on the current device's SM count.
+ * --------------------------------------------------------------------------- */
+
+/* Bytes of workspace a GEMV / linear launch of this shape needs on the current device (0 if invalid). */
+WOQ_API size_t woq_workspace_bytes(int bits, int M, int N, int K);
+
+/* Zero-fill a workspace on the stream (cudaMemsetAsync). */
+WOQ_API int woq_workspace_init(void* ws_dev, size_t ws_bytes, woq_stream_t stream);
+
+/* Synchronously read (and optionally clear) the workspace status word
+ * (WOQ_DEVERR_* bits).  Synchronises the stream. */
+WOQ_API int woq_read_status(void* ws_dev, size_t ws_bytes, int clear, uint32_t* status_out, woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Activation quantisation (section "Optimizing the Linear Kernel": the
+ * activation is quantised before the integer linear).
+ *   x_bf16: device bf16 [M][K]; q: device int8 [M][K]; ascale: device fp32 [M].
+ *   Per row: amax = max |x|, ascale = amax / 127 (IEEE division), q = round half
+ *   to even of x / ascale (IEEE division), clamped to [-127, 127]; a zero row
+ *   gives ascale 0 and q 0.  0 <= M <= woq_max_m(), K >= 0.  Non-finite x is
+ *   outside the domain (results undefined).
+ * --------------------------------------------------------------------------- */
+WOQ_API int woq_act_quant_int8(const void* x_bf16, int M, int K, int8_t* q, float* ascale, woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Skinny GEMV from int8 activations (sections "What is the bottleneck?" and
+ * "Optimizing the Linear Kernel").
+ *   wpacked: device, woq_packed_bytes(bits, N, K) bytes from the packer;
+ *   q: device int8 [M][K]; ascale: device fp32 [M] (from woq_act_quant_int8);
+ *   y: device fp32 [M][N], row-major, overwritten;
+ *   ws: device workspace of woq_workspace_bytes(bits, M, N, K) bytes.
+ *   0 <= M <= woq_max_m(); N >= 0; K >= 0, K % 128 == 0; M * K <= 98304 (the
+ *   activation tile lives in shared memory for the whole launch).
+ * --------------------------------------------------------------------------- */
+WOQ_API int woq_w4a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
+                  int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream);
+WOQ_API int woq_w6a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
+                  int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The whole linear in one launch from bf16 activations: every CTA quantises x
+ * exactly as woq_act_quant_int8 does, then runs the GEMV.  Bit-identical to
+ * woq_act_quant_int8 followed by woq_w?a8_gemv.  Same arguments and bounds as
+ * the GEMV, with x_bf16 (device bf16 [M][K]) in place of q and ascale.
+ * --------------------------------------------------------------------------- */
+WOQ_API int woq_w4a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K, float* y,
+                         void* ws, size_t ws_bytes, woq_stream_t stream);
+WOQ_API int woq_w6a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K, float* y,
+                         void* ws, size_t ws_bytes, woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Debug: the exact per-group integer dot products the GEMV scales.
+ *   dots: device int32 [M][N][K/128]; dots[m][n][g] = sum over k in group g of
+ *   w(n, k) * q(m, k).  Same bounds as the GEMV (no workspace).
+ * --------------------------------------------------------------------------- */
+WOQ_API int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_bytes, const int8_t* q, int M, int N, int K,
+                         int32_t* dots, woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Tuning: override the launch table for the following GEMV / linear launches
+ * of this process (ctas_per_sm in {1, 2}, stages in [2, 8]; 0 keeps the
+ * table's choice).  Not thread-safe; meant for benchmark sweeps.  Returns
+ * WOQ_ERR_SHAPE for values out of range.
+ * --------------------------------------------------------------------------- */
+WOQ_API int woq_tune_override(int ctas_per_sm, int stages);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WOQ_H */

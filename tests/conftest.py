@@ -1,4 +1,5 @@
 import os
+import subprocess
 import sys
 
 import pytest
@@ -10,3 +11,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
+
+
+def pytest_sessionstart(session):
+    # Build the CUDA library (nvcc cross-compiles without a GPU) and the oracle when stale.
+    # The build script runs as a program so that a missing library does not break the import.
+    subprocess.run([sys.executable, os.path.join(ROOT, "weight_only_quantised_gb300", "_build.py")], check=True,
+                   stdout=subprocess.DEVNULL)
+    import oracle
+    oracle.build()

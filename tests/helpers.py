@@ -35,7 +35,7 @@ def read_golden(name: str) -> dict:
 def encode_w4(vals: np.ndarray) -> np.ndarray:
     """int values in [-8, 7], shape [N, K] -> canonical bytes [N, K/2] (low nibble = even k)."""
     v = np.asarray(vals, dtype=np.int64)
-    assert v.min() >= -8 and v.max() <= 7
+    assert v.size == 0 or (v.min() >= -8 and v.max() <= 7)
     u = (v & 0xF).astype(np.uint8)
     return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
 
@@ -43,7 +43,7 @@ def encode_w4(vals: np.ndarray) -> np.ndarray:
 def encode_w6(vals: np.ndarray) -> np.ndarray:
     """int values in [-32, 31], shape [N, K] -> canonical bytes [N, 3K/4] (24-bit LE words of 4 fields)."""
     v = np.asarray(vals, dtype=np.int64)
-    assert v.min() >= -32 and v.max() <= 31
+    assert v.size == 0 or (v.min() >= -32 and v.max() <= 31)
     N, K = v.shape
     f = (v & 0x3F).reshape(N, K // 4, 4)
     word = f[..., 0] | (f[..., 1] << 6) | (f[..., 2] << 12) | (f[..., 3] << 18)

@@ -1,0 +1,210 @@
+"""Python binding of libwoq.so, the weight-only-quantised skinny linear for GB300.
+
+Argument marshalling only: every function forwards to the C ABI of the same
+name declared in include/woq.h, passing raw pointers (torch tensors'
+``data_ptr()`` for device buffers, numpy arrays for host buffers), sizes and the
+current CUDA stream.  Every step of the computation runs in the library's CUDA
+kernels; there is no Python or CPU fallback.  Importing this package loads the
+in-tree ``libwoq.so`` and raises if it has not been built
+(``python -m weight_only_quantised_gb300._build`` or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libwoq.so")
+
+WOQ_OK = 0
+WOQ_ERR_NULL = 1
+WOQ_ERR_ALIGN = 2
+WOQ_ERR_SHAPE = 3
+WOQ_ERR_WORKSPACE = 4
+WOQ_ERR_LAYOUT = 5
+WOQ_ERR_CUDA = 6
+WOQ_ERR_DEVICE = 7
+WOQ_DEVERR_HEADER = 0x1
+WOQ_DEVERR_TIMEOUT = 0x2
+GROUP = 128
+TILE_ROWS = 128
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it first (python -m weight_only_quantised_gb300._build)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_Z = ctypes.c_size_t
+_SIGS = {
+    "woq_version": ([], _I),
+    "woq_status_string": ([_I], ctypes.c_char_p),
+    "woq_max_m": ([], _I),
+    "woq_packed_bytes": ([_I, _I, _I], _Z),
+    "woq_pack_w4": ([_P, _P, _I, _I, _P, _Z], _I),
+    "woq_pack_w6": ([_P, _P, _I, _I, _P, _Z], _I),
+    "woq_unpack": ([_I, _P, _Z, _I, _I, _P, _P], _I),
+    "woq_pack_device": ([_I, _P, _P, _I, _I, _P, _Z, _P], _I),
+    "woq_workspace_bytes": ([_I, _I, _I, _I], _Z),
+    "woq_workspace_init": ([_P, _Z, _P], _I),
+    "woq_read_status": ([_P, _Z, _I, ctypes.POINTER(ctypes.c_uint32), _P], _I),
+    "woq_act_quant_int8": ([_P, _I, _I, _P, _P, _P], _I),
+    "woq_w4a8_gemv": ([_P, _Z, _P, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "woq_w6a8_gemv": ([_P, _Z, _P, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "woq_w4a8_linear_bf16": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "woq_w6a8_linear_bf16": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "woq_debug_group_dots": ([_I, _P, _Z, _P, _I, _I, _I, _P, _P], _I),
+    "woq_tune_override": ([_I, _I], _I),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+
+class WoqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {lib.woq_status_string(status).decode()} (status {status})")
+
+
+def _check(status: int, what: str) -> None:
+    if status != WOQ_OK:
+        raise WoqError(status, what)
+
+
+def _dptr(t):
+    """Device pointer of a tensor (None -> NULL)."""
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _hptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+# ----------------------------------------------------------------------------- info
+
+def woq_version() -> int:
+    return lib.woq_version()
+
+
+def woq_max_m() -> int:
+    return lib.woq_max_m()
+
+
+def woq_packed_bytes(bits: int, N: int, K: int) -> int:
+    return lib.woq_packed_bytes(bits, N, K)
+
+
+def woq_workspace_bytes(bits: int, M: int, N: int, K: int) -> int:
+    return lib.woq_workspace_bytes(bits, M, N, K)
+
+
+# ----------------------------------------------------------------------------- packing
+
+def _pack_host(fn, bits: int, q: np.ndarray, scales_f16: np.ndarray, N: int, K: int) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(scales_f16).view(np.uint16)
+    out = np.empty(max(lib.woq_packed_bytes(bits, N, K), 1), dtype=np.uint8)
+    _check(fn(_hptr(q), _hptr(s), N, K, _hptr(out), out.nbytes), fn.__name__)
+    return out[: lib.woq_packed_bytes(bits, N, K)]
+
+
+def woq_pack_w4(q4: np.ndarray, scales_f16: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Host pack: canonical int4 bytes [N, K/2] + fp16 scale bits [N, K/128] -> packed bytes."""
+    return _pack_host(lib.woq_pack_w4, 4, q4, scales_f16, N, K)
+
+
+def woq_pack_w6(q6: np.ndarray, scales_f16: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Host pack: canonical int6 bytes [N, 3K/4] + fp16 scale bits [N, K/128] -> packed bytes."""
+    return _pack_host(lib.woq_pack_w6, 6, q6, scales_f16, N, K)
+
+
+def woq_unpack(bits: int, packed: np.ndarray, N: int, K: int):
+    """Host unpack: packed bytes -> (canonical bytes [N, row bytes], fp16 scale bits [N, K/128])."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    row = K // 2 if bits == 4 else K // 4 * 3
+    q = np.zeros((N, row), dtype=np.uint8)
+    s = np.zeros((N, K // GROUP), dtype=np.uint16)
+    _check(lib.woq_unpack(bits, _hptr(packed), packed.nbytes, N, K, _hptr(q), _hptr(s)), "woq_unpack")
+    return q, s
+
+
+def woq_pack_device(bits: int, q_dev, scales_dev, N: int, K: int, dst_dev, stream=None) -> None:
+    """Device pack into dst_dev (uint8 tensor of woq_packed_bytes(bits, N, K) bytes)."""
+    _check(lib.woq_pack_device(bits, _dptr(q_dev), _dptr(scales_dev), N, K, _dptr(dst_dev), _nbytes(dst_dev),
+                               _stream(stream)), "woq_pack_device")
+
+
+# ----------------------------------------------------------------------------- workspace
+
+def woq_workspace_init(ws, stream=None) -> None:
+    _check(lib.woq_workspace_init(_dptr(ws), _nbytes(ws), _stream(stream)), "woq_workspace_init")
+
+
+def woq_read_status(ws, clear: bool = False, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(lib.woq_read_status(_dptr(ws), _nbytes(ws), int(clear), ctypes.byref(v), _stream(stream)),
+           "woq_read_status")
+    return int(v.value)
+
+
+# ----------------------------------------------------------------------------- compute
+
+def woq_act_quant_int8(x_bf16, q, ascale, stream=None) -> None:
+    """x_bf16 [M, K] bf16 -> q [M, K] int8, ascale [M] fp32 (device tensors)."""
+    M, K = x_bf16.shape
+    _check(lib.woq_act_quant_int8(_dptr(x_bf16), M, K, _dptr(q), _dptr(ascale), _stream(stream)),
+           "woq_act_quant_int8")
+
+
+def _gemv(fn, name, wpacked, q, ascale, N, K, y, ws, stream):
+    M = q.shape[0]
+    _check(fn(_dptr(wpacked), _nbytes(wpacked), _dptr(q), _dptr(ascale), M, N, K, _dptr(y), _dptr(ws), _nbytes(ws),
+              _stream(stream)), name)
+
+
+def woq_w4a8_gemv(wpacked, q, ascale, N: int, K: int, y, ws, stream=None) -> None:
+    _gemv(lib.woq_w4a8_gemv, "woq_w4a8_gemv", wpacked, q, ascale, N, K, y, ws, stream)
+
+
+def woq_w6a8_gemv(wpacked, q, ascale, N: int, K: int, y, ws, stream=None) -> None:
+    _gemv(lib.woq_w6a8_gemv, "woq_w6a8_gemv", wpacked, q, ascale, N, K, y, ws, stream)
+
+
+def _linear(fn, name, wpacked, x_bf16, N, K, y, ws, stream):
+    M = x_bf16.shape[0]
+    _check(fn(_dptr(wpacked), _nbytes(wpacked), _dptr(x_bf16), M, N, K, _dptr(y), _dptr(ws), _nbytes(ws),
+              _stream(stream)), name)
+
+
+def woq_w4a8_linear_bf16(wpacked, x_bf16, N: int, K: int, y, ws, stream=None) -> None:
+    _linear(lib.woq_w4a8_linear_bf16, "woq_w4a8_linear_bf16", wpacked, x_bf16, N, K, y, ws, stream)
+
+
+def woq_w6a8_linear_bf16(wpacked, x_bf16, N: int, K: int, y, ws, stream=None) -> None:
+    _linear(lib.woq_w6a8_linear_bf16, "woq_w6a8_linear_bf16", wpacked, x_bf16, N, K, y, ws, stream)
+
+
+def woq_debug_group_dots(bits: int, wpacked, q, N: int, K: int, dots, stream=None) -> None:
+    M = q.shape[0]
+    _check(lib.woq_debug_group_dots(bits, _dptr(wpacked), _nbytes(wpacked), _dptr(q), M, N, K, _dptr(dots),
+                                    _stream(stream)), "woq_debug_group_dots")
+
+
+def woq_tune_override(ctas_per_sm: int = 0, stages: int = 0) -> None:
+    _check(lib.woq_tune_override(ctas_per_sm, stages), "woq_tune_override")

@@ -1,0 +1,259 @@
+// C ABI of the skinny linear: argument validation, the per-shape launch table
+// and the device entry points.  Everything here is host code; every step of
+// the computation runs in the kernels of woq_gemv.cuh and woq_small_kernels.cu.
+#include <atomic>
+#include <mutex>
+
+#include "../../include/woq.h"
+#include "woq_gemv_launch.cuh"
+#include "woq_internal.h"
+#include "woq_layout.h"
+
+namespace woq {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_max_smem[kMaxDevices];
+std::atomic<int> g_override_cps{0};
+std::atomic<int> g_override_stages{0};
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+int sm_count() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 0;
+  int v = g_sm_count[d].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+    g_sm_count[d].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+int max_dynamic_smem() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 0;
+  int v = g_max_smem[d].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) != cudaSuccess) return 0;
+    g_max_smem[d].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+// [barriers, flags: 256][reduction buffers][activations M x K int8][ring]
+static int red_bytes(int M) { return 2 * kConsumerWarps * M * kTileRows * 4; }
+static int act_offset(int M) { return 256 + red_bytes(M); }
+static int ring_offset(int M, int K) { return (int)align_up((size_t)act_offset(M) + (size_t)M * K, 128); }
+
+int smem_bytes_for(int bits, int M, int K, int stages) {
+  return ring_offset(M, K) + stages * kConsumerWarps * block_bytes(bits);
+}
+
+LaunchConfig choose_config(int bits, int M, int N, int K) {
+  LaunchConfig cfg = {0, 0, 0};
+  const int sms = sm_count();
+  const int smem_max = max_dynamic_smem();
+  if (sms <= 0 || smem_max <= 0) return cfg;
+  const long long T = (N + kTileRows - 1) / kTileRows;
+  const long long G = K / kGroup;
+  const long long NB = T * G;
+  if (NB <= 0) return cfg;
+  int cps = g_override_cps.load(std::memory_order_relaxed);
+  if (cps <= 0) cps = 1;
+  // per-CTA shared memory budget: one CTA gets the opt-in maximum; two share the SM's 228 KB
+  const int budget = cps == 1 ? smem_max : (233472 - cps * 1024) / cps;
+  int stages = g_override_stages.load(std::memory_order_relaxed);
+  if (stages <= 0) stages = 4;
+  while (stages >= 2 && smem_bytes_for(bits, M, K, stages) > budget) --stages;
+  if (stages < 2) return cfg;
+  // at least one stage (kConsumerWarps blocks) of work per CTA
+  long long ctas = (long long)sms * cps;
+  const long long by_work = (NB + kConsumerWarps - 1) / kConsumerWarps;
+  if (ctas > by_work) ctas = by_work;
+  if (ctas < 1) ctas = 1;
+  cfg.ctas = (int)ctas;
+  cfg.stages = stages;
+  cfg.smem_bytes = smem_bytes_for(bits, M, K, stages);
+  return cfg;
+}
+
+WorkspaceLayout workspace_layout(int M, int N, int ctas) {
+  WorkspaceLayout wl;
+  const size_t T = (size_t)(N + kTileRows - 1) / kTileRows;
+  wl.tickets_offset = 256;
+  wl.partials_offset = align_up(wl.tickets_offset + T * 4, 256);
+  wl.total = wl.partials_offset + (size_t)ctas * 2 * (size_t)M * kTileRows * 4;
+  return wl;
+}
+
+// workspace is sized for the largest grid the table or an override may pick
+static int max_ctas_for_workspace() { return 2 * sm_count(); }
+
+}  // namespace woq
+
+using namespace woq;
+
+extern "C" {
+
+int woq_version(void) { return 100; }
+
+int woq_max_m(void) { return kMaxM; }
+
+const char* woq_status_string(int status) {
+  switch (status) {
+    case WOQ_OK: return "ok";
+    case WOQ_ERR_NULL: return "a required pointer is NULL";
+    case WOQ_ERR_ALIGN: return "a device pointer is not suitably aligned";
+    case WOQ_ERR_SHAPE: return "M, N, K or bits outside the supported range";
+    case WOQ_ERR_WORKSPACE: return "workspace smaller than woq_workspace_bytes()";
+    case WOQ_ERR_LAYOUT: return "packed buffer size or header does not match (bits, N, K)";
+    case WOQ_ERR_CUDA: return "a CUDA runtime call failed";
+    case WOQ_ERR_DEVICE: return "a kernel reported an error in the workspace status word";
+    default: return "unknown status";
+  }
+}
+
+int woq_tune_override(int ctas_per_sm, int stages) {
+  if (ctas_per_sm < 0 || ctas_per_sm > 2 || stages < 0 || stages == 1 || stages > kMaxStages) return WOQ_ERR_SHAPE;
+  g_override_cps.store(ctas_per_sm);
+  g_override_stages.store(stages);
+  return WOQ_OK;
+}
+
+size_t woq_workspace_bytes(int bits, int M, int N, int K) {
+  if ((bits != 4 && bits != 6) || M < 0 || M > kMaxM || N < 0 || K < 0 || K % kGroup) return 0;
+  if (M == 0 || N == 0 || K == 0) return 256;  // empty shapes launch nothing
+  const int c = max_ctas_for_workspace();
+  if (c <= 0) return 0;
+  return workspace_layout(M, N, c).total;
+}
+
+int woq_workspace_init(void* ws_dev, size_t ws_bytes, woq_stream_t stream) {
+  if (!ws_dev) return WOQ_ERR_NULL;
+  if (!aligned(ws_dev, 16)) return WOQ_ERR_ALIGN;
+  return cudaMemsetAsync(ws_dev, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+}
+
+int woq_read_status(void* ws_dev, size_t ws_bytes, int clear, uint32_t* status_out, woq_stream_t stream) {
+  if (!ws_dev || !status_out) return WOQ_ERR_NULL;
+  if (ws_bytes < 4) return WOQ_ERR_WORKSPACE;
+  uint32_t v = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&v, ws_dev, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return WOQ_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return WOQ_ERR_CUDA;
+  if (clear && v) {
+    if (cudaMemsetAsync(ws_dev, 0, 4, s) != cudaSuccess) return WOQ_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return WOQ_ERR_CUDA;
+  }
+  *status_out = v;
+  return WOQ_OK;
+}
+
+int woq_pack_device(int bits, const uint8_t* q_dev, const uint16_t* scales_dev, int N, int K, void* dst_dev,
+                    size_t dst_bytes, woq_stream_t stream) {
+  const size_t need = packed_bytes(bits, N, K);
+  if (need == 0) return WOQ_ERR_SHAPE;
+  if (!dst_dev || ((!q_dev || !scales_dev) && (size_t)N * (size_t)K > 0)) return WOQ_ERR_NULL;
+  if (!aligned(dst_dev, 16) || !aligned(q_dev, 16) || !aligned(scales_dev, 2)) return WOQ_ERR_ALIGN;
+  if (dst_bytes < need) return WOQ_ERR_LAYOUT;
+  return launch_pack_device(bits, q_dev, scales_dev, N, K, dst_dev, (cudaStream_t)stream) == cudaSuccess
+             ? WOQ_OK
+             : WOQ_ERR_CUDA;
+}
+
+int woq_act_quant_int8(const void* x_bf16, int M, int K, int8_t* q, float* ascale, woq_stream_t stream) {
+  if (M < 0 || M > kMaxM || K < 0) return WOQ_ERR_SHAPE;
+  if (M == 0) return WOQ_OK;
+  if (!ascale || (K > 0 && (!x_bf16 || !q))) return WOQ_ERR_NULL;
+  if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(ascale, 4)) return WOQ_ERR_ALIGN;
+  return launch_act_quant(x_bf16, M, K, q, ascale, (cudaStream_t)stream) == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+}
+
+static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_bytes, const void* x_bf16,
+                    const int8_t* q, const float* ascale, int M, int N, int K, float* y, void* ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+  if (M < 0 || M > kMaxM || N < 0 || K < 0 || K % kGroup || (long)M * K > kMaxMK) return WOQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return WOQ_OK;  // nothing to compute
+  if (!y) return WOQ_ERR_NULL;
+  if (!aligned(y, 4)) return WOQ_ERR_ALIGN;
+  if (K == 0) {  // no groups: every output is the empty sum
+    return cudaMemsetAsync(y, 0, (size_t)M * N * sizeof(float), stream) == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+  }
+  if (!wpacked || !ws) return WOQ_ERR_NULL;
+  if (fused ? !x_bf16 : (!q || !ascale)) return WOQ_ERR_NULL;
+  if (!aligned(wpacked, 16) || !aligned(y, 4) || !aligned(ws, 16)) return WOQ_ERR_ALIGN;
+  if (fused ? !aligned(x_bf16, 16) : (!aligned(q, 16) || !aligned(ascale, 4))) return WOQ_ERR_ALIGN;
+  if (wpacked_bytes < packed_bytes(bits, N, K)) return WOQ_ERR_LAYOUT;
+  const LaunchConfig cfg = choose_config(bits, M, N, K);
+  if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
+  const WorkspaceLayout wl = workspace_layout(M, N, cfg.ctas);
+  if (ws_bytes < wl.total || cfg.ctas > max_ctas_for_workspace()) return WOQ_ERR_WORKSPACE;
+  GemvParams p;
+  p.w = static_cast<const uint8_t*>(wpacked);
+  p.x = static_cast<const uint16_t*>(x_bf16);
+  p.q = q;
+  p.ascale = ascale;
+  p.y = y;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  p.status = reinterpret_cast<uint32_t*>(wsb);
+  p.tickets = reinterpret_cast<uint32_t*>(wsb + wl.tickets_offset);
+  p.partials = reinterpret_cast<float*>(wsb + wl.partials_offset);
+  p.N = N;
+  p.K = K;
+  p.T = (N + kTileRows - 1) / kTileRows;
+  p.G = K / kGroup;
+  p.NB = (long long)p.T * p.G;
+  p.stages = cfg.stages;
+  p.act_offset = act_offset(M);
+  p.red_offset = 256;
+  p.ring_offset = ring_offset(M, K);
+  const cudaError_t e = bits == 4 ? launch_gemv_w4(fused, M, p, cfg, stream) : launch_gemv_w6(fused, M, p, cfg, stream);
+  return e == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+}
+
+int woq_w4a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
+                  int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream) {
+  return run_gemv(4, false, wpacked, wpacked_bytes, nullptr, q, ascale, M, N, K, y, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int woq_w6a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
+                  int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream) {
+  return run_gemv(6, false, wpacked, wpacked_bytes, nullptr, q, ascale, M, N, K, y, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int woq_w4a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K, float* y,
+                         void* ws, size_t ws_bytes, woq_stream_t stream) {
+  return run_gemv(4, true, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, M, N, K, y, ws, ws_bytes,
+                  (cudaStream_t)stream);
+}
+
+int woq_w6a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K, float* y,
+                         void* ws, size_t ws_bytes, woq_stream_t stream) {
+  return run_gemv(6, true, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, M, N, K, y, ws, ws_bytes,
+                  (cudaStream_t)stream);
+}
+
+int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_bytes, const int8_t* q, int M, int N, int K,
+                         int32_t* dots, woq_stream_t stream) {
+  if ((bits != 4 && bits != 6) || M < 0 || M > kMaxM || N < 0 || K < 0 || K % kGroup) return WOQ_ERR_SHAPE;
+  if (M == 0 || N == 0 || K == 0) return WOQ_OK;  // no groups or no outputs
+  if (!wpacked || !q || !dots) return WOQ_ERR_NULL;
+  if (!aligned(wpacked, 16) || !aligned(q, 16) || !aligned(dots, 4)) return WOQ_ERR_ALIGN;
+  if (wpacked_bytes < packed_bytes(bits, N, K)) return WOQ_ERR_LAYOUT;
+  return launch_group_dots(bits, wpacked, q, M, N, K, dots, (cudaStream_t)stream) == cudaSuccess ? WOQ_OK
+                                                                                                  : WOQ_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,10 @@
+// Instantiations of the skinny GEMV / linear kernel for int4 weights.
+#include "woq_gemv_launch.cuh"
+
+namespace woq {
+
+cudaError_t launch_gemv_w4(bool fused, int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream) {
+  return launch_gemv_bits<4>(fused, M, p, cfg, stream);
+}
+
+}  // namespace woq

@@ -1,0 +1,48 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime.h>
+
+namespace woq {
+
+void write_header(void* dst, int bits, int N, int K);
+bool header_matches(const void* src, int bits, int N, int K);
+
+// Launch configuration of one GEMV / linear launch (chosen by the launch table).
+struct LaunchConfig {
+  int ctas;         // grid size (CTAs); each CTA streams an equal share of the blocks
+  int stages;       // ring stages of kConsumerWarps blocks each
+  int smem_bytes;   // dynamic shared memory per CTA
+};
+
+// Workspace layout: [status word + pad: 256 B][tickets: uint32 per tile, padded to 256 B][partials]
+struct WorkspaceLayout {
+  size_t tickets_offset;
+  size_t partials_offset;
+  size_t total;
+};
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+
+int sm_count();                       // SMs of the current device (cached per device)
+int max_dynamic_smem();               // opt-in shared memory per block of the current device
+int smem_bytes_for(int bits, int M, int K, int stages);
+LaunchConfig choose_config(int bits, int M, int N, int K);
+WorkspaceLayout workspace_layout(int M, int N, int ctas);
+
+// Kernel launchers (woq_gemv.cu); return a cudaError_t.
+cudaError_t launch_gemv(int bits, bool fused, int M, int N, int K, const void* wpacked, const void* x_bf16,
+                        const int8_t* q, const float* ascale, float* y, void* ws, const LaunchConfig& cfg,
+                        const WorkspaceLayout& wl, cudaStream_t stream);
+cudaError_t launch_act_quant(const void* x_bf16, int M, int K, int8_t* q, float* ascale, cudaStream_t stream);
+cudaError_t launch_group_dots(int bits, const void* wpacked, const int8_t* q, int M, int N, int K, int32_t* dots,
+                              cudaStream_t stream);
+cudaError_t launch_pack_device(int bits, const uint8_t* q, const uint16_t* scales, int N, int K, void* dst,
+                               cudaStream_t stream);
+
+}  // namespace woq

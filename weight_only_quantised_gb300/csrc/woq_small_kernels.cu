@@ -1,0 +1,271 @@
+// Small kernels: standalone activation quantisation, the debug group-dot
+// kernel and the device-side packer.
+#include <cuda_fp16.h>
+
+#include "woq_device.cuh"
+#include "woq_gemv.cuh"
+#include "woq_internal.h"
+#include "woq_layout.h"
+
+namespace woq {
+namespace kern {
+
+// ---------------------------------------------------------------------------
+// Activation quantisation ("Optimizing the Linear Kernel": the activation is
+// quantised to int8 before the linear).  One CTA per row:
+// amax = max |x|; s = amax / 127 (IEEE); q = rne(x / s) (IEEE), clamped to
+// [-127, 127]; a zero row gives s = 0 and q = 0.
+// ---------------------------------------------------------------------------
+constexpr int kAqThreads = 1024;
+
+__device__ __forceinline__ int8_t quant_one(float x, float s) {
+  if (s == 0.0f) return 0;
+  const float r = rintf(__fdiv_rn(x, s));
+  return (int8_t)(int)fminf(fmaxf(r, -127.0f), 127.0f);
+}
+
+__global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint16_t* __restrict__ x, int K,
+                                                               int8_t* __restrict__ q, float* __restrict__ ascale) {
+  __shared__ float s_part[kAqThreads / 32];
+  dev::pdl_launch_dependents();
+  dev::pdl_wait_prior_grids();
+  const int m = blockIdx.x;
+  const int tid = threadIdx.x;
+  const uint16_t* xr = x + (size_t)m * K;
+  int8_t* qr = q + (size_t)m * K;
+  const bool vec = (K % 8) == 0;
+  float amax = 0.0f;
+  if (vec) {
+    for (int e = tid * 8; e < K; e += kAqThreads * 8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + e));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(dev::bf16_bits_to_float(w[i] & 0xFFFFu)));
+        amax = fmaxf(amax, fabsf(dev::bf16_bits_to_float(w[i] >> 16)));
+      }
+    }
+  } else {
+    for (int e = tid; e < K; e += kAqThreads) amax = fmaxf(amax, fabsf(dev::bf16_bits_to_float(xr[e])));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((tid & 31) == 0) s_part[tid >> 5] = amax;
+  __syncthreads();
+  amax = s_part[0];
+  for (int i = 1; i < kAqThreads / 32; ++i) amax = fmaxf(amax, s_part[i]);
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (tid == 0) ascale[m] = s;
+  if (vec) {
+    for (int e = tid * 8; e < K; e += kAqThreads * 8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + e));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t b16 = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
+        packed[i >> 2] |= ((uint32_t)(uint8_t)quant_one(dev::bf16_bits_to_float(b16), s)) << (8 * (i & 3));
+      }
+      *reinterpret_cast<uint2*>(qr + e) = make_uint2(packed[0], packed[1]);
+    }
+  } else {
+    for (int e = tid; e < K; e += kAqThreads) qr[e] = quant_one(dev::bf16_bits_to_float(xr[e]), s);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Debug: exact per-group dot products straight from the packed layout.
+// One thread per (row n, group g); dots[m][n][g].
+// ---------------------------------------------------------------------------
+template <int BITS, int M>
+__global__ void group_dots_kernel(const uint8_t* __restrict__ w, const int8_t* __restrict__ q, int N, int K,
+                                  int32_t* __restrict__ dots) {
+  constexpr int BB = Fmt<BITS>::kBlockBytes;
+  const int G = K / kGroup;
+  const long long total = (long long)N * G;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int n = (int)(idx / G);
+    const int g = (int)(idx % G);
+    const int t = n / kTileRows, r = n % kTileRows, j = r / 32, l = r % 32;
+    const uint8_t* blk = w + kHeaderBytes + ((size_t)t * G + g) * BB;
+    int d[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) d[m] = 0;
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(blk + kScaleBytes + ((c * 4 + j) * 32 + l) * 16));
+      uint2 u = make_uint2(0u, 0u);
+      if constexpr (BITS == 6)
+        u = __ldg(reinterpret_cast<const uint2*>(blk + kScaleBytes + kW4Bytes + ((c * 4 + j) * 32 + l) * 8));
+      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t lo, hi;
+        unpack_word<BITS>(vw[i], (i < 2) ? u.x : u.y, i & 1, lo, hi);
+        const int k0 = g * kGroup + 32 * c + 8 * i;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const uint2 a = __ldg(reinterpret_cast<const uint2*>(q + (size_t)m * K + k0));
+          d[m] = dev::dp4a_ss(lo, a.x, d[m]);
+          d[m] = dev::dp4a_ss(hi, a.y, d[m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) dots[((size_t)m * N + n) * G + g] = BITS == 4 ? (d[m] >> 4) : (d[m] >> 2);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Device packer: one thread per (tile, group, quarter c, row group j, lane l)
+// chunk; writes the same bytes as the host packer.
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ scales, int N, int K, int T,
+                            uint8_t* __restrict__ dst, PackedHeader hdr) {
+  constexpr int BB = Fmt<BITS>::kBlockBytes;
+  const int G = K / kGroup;
+  const long long total = (long long)T * G * 512;
+  if (blockIdx.x == 0 && threadIdx.x < kHeaderBytes / 4) {
+    uint32_t word = 0;
+    if (threadIdx.x * 4 < (int)sizeof(PackedHeader)) memcpy(&word, reinterpret_cast<const uint8_t*>(&hdr) + threadIdx.x * 4, 4);
+    reinterpret_cast<uint32_t*>(dst)[threadIdx.x] = word;
+  }
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int l = (int)(idx & 31);
+    const int j = (int)((idx >> 5) & 3);
+    const int c = (int)((idx >> 7) & 3);
+    const long long tg = idx >> 9;
+    const int g = (int)(tg % G);
+    const long long t = tg / G;
+    const long long n = t * kTileRows + 32 * j + l;
+    uint8_t* blk = dst + kHeaderBytes + (size_t)tg * BB;
+    uint32_t lo[4] = {0u, 0u, 0u, 0u};
+    uint32_t hi[2] = {0u, 0u};
+    if (n < N) {
+      const int kb = g * kGroup + 32 * c;
+      uint8_t code[32];
+      if constexpr (BITS == 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + (size_t)n * (K / 2) + kb / 2));
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk) code[kk] = (uint8_t)((vw[kk >> 3] >> (4 * (kk & 7))) & 0xF);
+      } else {
+        const uint8_t* src = q + (size_t)n * (K / 4 * 3) + (size_t)(kb / 4) * 3;
+        const uint2 a = __ldg(reinterpret_cast<const uint2*>(src));
+        const uint2 b = __ldg(reinterpret_cast<const uint2*>(src + 8));
+        const uint2 cc = __ldg(reinterpret_cast<const uint2*>(src + 16));
+        const uint32_t bw[6] = {a.x, a.y, b.x, b.y, cc.x, cc.y};
+#pragma unroll
+        for (int quad = 0; quad < 8; ++quad) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int byte = 0; byte < 3; ++byte) {
+            const int pos = quad * 3 + byte;
+            word |= ((bw[pos >> 2] >> (8 * (pos & 3))) & 0xFFu) << (8 * byte);
+          }
+#pragma unroll
+          for (int f = 0; f < 4; ++f) code[quad * 4 + f] = (uint8_t)((word >> (6 * f)) & 0x3F);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint8_t ca = code[8 * i + b], cb = code[8 * i + 4 + b];
+          lo[i] |= ((uint32_t)(ca & 0xF) | ((uint32_t)(cb & 0xF) << 4)) << (8 * b);
+          if constexpr (BITS == 6) {
+            const int h = i >> 1, e = i & 1;
+            hi[h] |= ((uint32_t)((ca >> 4) & 3) << (2 * (2 * e))) << (8 * b);
+            hi[h] |= ((uint32_t)((cb >> 4) & 3) << (2 * (2 * e + 1))) << (8 * b);
+          }
+        }
+    }
+    *reinterpret_cast<uint4*>(blk + kScaleBytes + ((c * 4 + j) * 32 + l) * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    if constexpr (BITS == 6)
+      *reinterpret_cast<uint2*>(blk + kScaleBytes + kW4Bytes + ((c * 4 + j) * 32 + l) * 8) = make_uint2(hi[0], hi[1]);
+    if (c == 0) {
+      const int r = 32 * j + l;
+      const uint16_t s = n < N ? scales[(size_t)n * G + g] : (uint16_t)0;
+      reinterpret_cast<uint16_t*>(blk)[scale_index(r)] = s;
+    }
+  }
+}
+
+}  // namespace kern
+
+static cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, cudaStream_t stream, void** args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = 0;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelExC(&lc, func, args);
+}
+
+cudaError_t launch_act_quant(const void* x_bf16, int M, int K, int8_t* q, float* ascale, cudaStream_t stream) {
+  const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+  void* args[] = {(void*)&x, (void*)&K, (void*)&q, (void*)&ascale};
+  return launch_pdl((const void*)kern::act_quant_kernel, dim3((unsigned)M), dim3(kern::kAqThreads), stream, args);
+}
+
+template <int BITS>
+static cudaError_t launch_dots_bits(const void* wpacked, const int8_t* q, int M, int N, int K, int32_t* dots,
+                                    cudaStream_t stream) {
+  const uint8_t* w = static_cast<const uint8_t*>(wpacked);
+  const long long total = (long long)N * (K / kGroup);
+  const int threads = 256;
+  const long long blocks_needed = (total + threads - 1) / threads;
+  const unsigned blocks = (unsigned)(blocks_needed < 65535 ? blocks_needed : 65535);
+  switch (M) {
+    case 1: kern::group_dots_kernel<BITS, 1><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
+    case 2: kern::group_dots_kernel<BITS, 2><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
+    case 3: kern::group_dots_kernel<BITS, 3><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
+    case 4: kern::group_dots_kernel<BITS, 4><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_dots(int bits, const void* wpacked, const int8_t* q, int M, int N, int K, int32_t* dots,
+                              cudaStream_t stream) {
+  return bits == 4 ? launch_dots_bits<4>(wpacked, q, M, N, K, dots, stream)
+                   : launch_dots_bits<6>(wpacked, q, M, N, K, dots, stream);
+}
+
+cudaError_t launch_pack_device(int bits, const uint8_t* q, const uint16_t* scales, int N, int K, void* dst,
+                               cudaStream_t stream) {
+  const int T = (N + kTileRows - 1) / kTileRows;
+  const int G = K / kGroup;
+  PackedHeader h;
+  memset(&h, 0, sizeof(h));
+  h.magic = kMagic;
+  h.version = kLayoutVersion;
+  h.bits = (uint32_t)bits;
+  h.tile_rows = kTileRows;
+  h.N = (uint32_t)N;
+  h.K = (uint32_t)K;
+  h.tiles = (uint32_t)T;
+  h.groups = (uint32_t)G;
+  h.block_bytes = (uint64_t)block_bytes(bits);
+  h.total_bytes = (uint64_t)packed_bytes(bits, N, K);
+  const long long total = (long long)T * G * 512;
+  const int threads = 256;
+  long long blocks_needed = (total + threads - 1) / threads;
+  if (blocks_needed < 1) blocks_needed = 1;
+  const unsigned blocks = (unsigned)(blocks_needed < 1048576 ? blocks_needed : 1048576);
+  uint8_t* d = static_cast<uint8_t*>(dst);
+  if (bits == 4)
+    kern::pack_kernel<4><<<blocks, threads, 0, stream>>>(q, scales, N, K, T, d, h);
+  else
+    kern::pack_kernel<6><<<blocks, threads, 0, stream>>>(q, scales, N, K, T, d, h);
+  return cudaGetLastError();
+}
+
+}  // namespace woq
