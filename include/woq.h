@@ -79,6 +79,12 @@ WOQ_API const char* woq_status_string(int status);
 /* Largest supported M (activation rows). */
 WOQ_API int woq_max_m(void);
 
+/* Largest supported K for a GEMV (fused = 0) or bf16 linear (fused = 1) launch with
+ * M activation rows on the current device: the activations stay in shared memory
+ * next to at least two ring stages (int8 entry: M * K bytes, M * K <= 98304; bf16
+ * entry: 2 * M * K bytes).  0 for invalid arguments. */
+WOQ_API int woq_max_k(int bits, int M, int fused);
+
 /* ---------------------------------------------------------------------------
  * Packing (section "Optimizing the Linear Kernel": weights and their
  * per-group scales are interleaved in the order the kernel consumes them, so
@@ -156,8 +162,8 @@ WOQ_API int woq_act_quant_int8(const void* x_bf16, int M, int K, int8_t* q, floa
  *   q: device int8 [M][K]; ascale: device fp32 [M] (from woq_act_quant_int8);
  *   y: device fp32 [M][N], row-major, overwritten;
  *   ws: device workspace of woq_workspace_bytes(bits, M, N, K) bytes.
- *   0 <= M <= woq_max_m(); N >= 0; K >= 0, K % 128 == 0; M * K <= 98304 (the
- *   activation tile lives in shared memory for the whole launch).
+ *   0 <= M <= woq_max_m(); N >= 0; K >= 0, K % 128 == 0; K <= woq_max_k(bits, M, 0)
+ *   (the activation tile lives in shared memory for the whole launch).
  * --------------------------------------------------------------------------- */
 WOQ_API int woq_w4a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
                   int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream);
@@ -167,8 +173,9 @@ WOQ_API int woq_w6a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_
 /* ---------------------------------------------------------------------------
  * The whole linear in one launch from bf16 activations: every CTA quantises x
  * exactly as woq_act_quant_int8 does, then runs the GEMV.  Bit-identical to
- * woq_act_quant_int8 followed by woq_w?a8_gemv.  Same arguments and bounds as
- * the GEMV, with x_bf16 (device bf16 [M][K]) in place of q and ascale.
+ * woq_act_quant_int8 followed by woq_w?a8_gemv.  Same arguments as the GEMV,
+ * with x_bf16 (device bf16 [M][K]) in place of q and ascale; K <= woq_max_k(bits, M, 1)
+ * (x is staged as bf16 in shared memory).
  * --------------------------------------------------------------------------- */
 WOQ_API int woq_w4a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K, float* y,
                          void* ws, size_t ws_bytes, woq_stream_t stream);
@@ -185,11 +192,13 @@ WOQ_API int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_b
 
 /* ---------------------------------------------------------------------------
  * Tuning: override the launch table for the following GEMV / linear launches
- * of this process (ctas_per_sm in {1, 2}, stages in [2, 8]; 0 keeps the
- * table's choice).  Not thread-safe; meant for benchmark sweeps.  Returns
- * WOQ_ERR_SHAPE for values out of range.
+ * of this process.  ctas_per_sm in {1, 2} (0 = table), stages in [2, 8]
+ * (0 = table), prefetch_kb = weight bytes per CTA kept in flight into L2
+ * beyond the shared-memory ring, in KiB (-1 = table, 0 = none).  Not
+ * thread-safe; meant for benchmark sweeps.  WOQ_ERR_SHAPE for values out of
+ * range.
  * --------------------------------------------------------------------------- */
-WOQ_API int woq_tune_override(int ctas_per_sm, int stages);
+WOQ_API int woq_tune_override(int ctas_per_sm, int stages, int prefetch_kb);
 
 #ifdef __cplusplus
 }

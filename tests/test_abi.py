@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
 
 def test_library_exports_every_declared_symbol(woq):
     names = declared_functions()
-    assert len(names) >= 18
+    assert len(names) >= 19
     for n in names:
         assert hasattr(woq.lib, n), n
     # and nothing else leaks out (the CUDA runtime is linked statically and kept local)
@@ -104,6 +104,7 @@ def test_linear_and_act_quant_host_validation(woq):
     assert L.woq_act_quant_int8(P(FAKE + 1), 1, 128, P(FAKE), P(FAKE), None) == woq.WOQ_ERR_ALIGN
     assert L.woq_debug_group_dots(5, P(FAKE), 10 ** 9, P(FAKE), 1, 128, 128, P(FAKE), None) == woq.WOQ_ERR_SHAPE
     assert L.woq_debug_group_dots(4, None, 10 ** 9, P(FAKE), 1, 128, 128, P(FAKE), None) == woq.WOQ_ERR_NULL
-    assert L.woq_tune_override(3, 0) == woq.WOQ_ERR_SHAPE
-    assert L.woq_tune_override(0, 1) == woq.WOQ_ERR_SHAPE
-    assert L.woq_tune_override(0, 0) == woq.WOQ_OK
+    assert L.woq_tune_override(3, 0, -1) == woq.WOQ_ERR_SHAPE
+    assert L.woq_tune_override(0, 1, -1) == woq.WOQ_ERR_SHAPE
+    assert L.woq_tune_override(0, 0, -2) == woq.WOQ_ERR_SHAPE
+    assert L.woq_tune_override(0, 0, -1) == woq.WOQ_OK

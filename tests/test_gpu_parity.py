@@ -28,7 +28,7 @@ def _gpu():
     woq = w
     torch.cuda.set_device(0)
     yield
-    woq.woq_tune_override(0, 0)
+    woq.woq_tune_override(0, 0, -1)
 
 
 DEV = "cuda:0"
@@ -215,8 +215,8 @@ def test_device_pack_matches_host_pack(bits, N, K):
     assert np.array_equal(dst.cpu().numpy(), host)
 
 
-@pytest.mark.parametrize("cps,stages", [(1, 2), (1, 3), (1, 4), (2, 2), (2, 3), (1, 8)])
-def test_launch_configurations_agree(cps, stages):
+@pytest.mark.parametrize("cps,stages,pf", [(1, 2, 0), (1, 3, -1), (1, 4, 1024), (2, 2, -1), (2, 3, 64), (1, 8, -1)])
+def test_launch_configurations_agree(cps, stages, pf):
     bits, M, N, K = 4, 2, 2048, 2048
     w, s = make_weights(bits, N, K, seed=21)
     wn, sn = to_numpy_u8(w), to_numpy_u16(s)
@@ -225,13 +225,31 @@ def test_launch_configurations_agree(cps, stages):
     y_ref, S = oracle.linear_bf16(bits, wn, sn, N, K, xn)
     wdev = pack_host(bits, wn, sn, N, K)
     x_dev = torch.from_numpy(xn.view(np.int16)).to(DEV).view(torch.bfloat16)
-    woq.woq_tune_override(cps, stages)
+    woq.woq_tune_override(cps, stages, pf)
     try:
         y = run_linear(bits, wdev, x_dev, N, K, M)
     finally:
-        woq.woq_tune_override(0, 0)
+        woq.woq_tune_override(0, 0, -1)
     ok, worst = tol_ok(y, y_ref, S)
     assert ok, f"max err / tolerance = {worst}"
+
+
+def test_max_k_bounds():
+    for bits in (4, 6):
+        for M in (1, 2, 3, 4):
+            k8, kb = woq.woq_max_k(bits, M, False), woq.woq_max_k(bits, M, True)
+            assert k8 % 128 == 0 and kb % 128 == 0 and 0 < kb <= k8 and M * k8 <= 98304
+    # the decode shapes of the 27B and 9B workloads fit the fused entry at M = 4
+    assert woq.woq_max_k(4, 4, True) >= 17408 and woq.woq_max_k(6, 4, True) >= 12288
+    # beyond the bound the call is refused on the host
+    K = woq.woq_max_k(4, 4, True) + 128
+    y = torch.empty((4, 128), device=DEV)
+    x = torch.empty((4, K), dtype=torch.bfloat16, device=DEV)
+    w = torch.empty(woq.woq_packed_bytes(4, 128, K), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(woq.woq_workspace_bytes(4, 4, 128, K), dtype=torch.uint8, device=DEV)
+    with pytest.raises(woq.WoqError) as e:
+        woq.woq_w4a8_linear_bf16(w, x, 128, K, y, ws)
+    assert e.value.status == woq.WOQ_ERR_SHAPE
 
 
 def test_header_mismatch_sets_status_and_leaves_y():

@@ -16,7 +16,8 @@ import os
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libwoq.so")
+# WOQ_LIB selects another build of the same ABI (e.g. the trace build libwoq_trace.so)
+LIB_PATH = os.environ.get("WOQ_LIB") or os.path.join(_PKG, "libwoq.so")
 
 WOQ_OK = 0
 WOQ_ERR_NULL = 1
@@ -43,6 +44,7 @@ _SIGS = {
     "woq_version": ([], _I),
     "woq_status_string": ([_I], ctypes.c_char_p),
     "woq_max_m": ([], _I),
+    "woq_max_k": ([_I, _I, _I], _I),
     "woq_packed_bytes": ([_I, _I, _I], _Z),
     "woq_pack_w4": ([_P, _P, _I, _I, _P, _Z], _I),
     "woq_pack_w6": ([_P, _P, _I, _I, _P, _Z], _I),
@@ -57,7 +59,7 @@ _SIGS = {
     "woq_w4a8_linear_bf16": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
     "woq_w6a8_linear_bf16": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
     "woq_debug_group_dots": ([_I, _P, _Z, _P, _I, _I, _I, _P, _P], _I),
-    "woq_tune_override": ([_I, _I], _I),
+    "woq_tune_override": ([_I, _I, _I], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -104,6 +106,10 @@ def woq_version() -> int:
 
 def woq_max_m() -> int:
     return lib.woq_max_m()
+
+
+def woq_max_k(bits: int, M: int, fused: bool) -> int:
+    return lib.woq_max_k(bits, M, int(fused))
 
 
 def woq_packed_bytes(bits: int, N: int, K: int) -> int:
@@ -206,5 +212,5 @@ def woq_debug_group_dots(bits: int, wpacked, q, N: int, K: int, dots, stream=Non
                                     _stream(stream)), "woq_debug_group_dots")
 
 
-def woq_tune_override(ctas_per_sm: int = 0, stages: int = 0) -> None:
-    _check(lib.woq_tune_override(ctas_per_sm, stages), "woq_tune_override")
+def woq_tune_override(ctas_per_sm: int = 0, stages: int = 0, prefetch_kb: int = -1) -> None:
+    _check(lib.woq_tune_override(ctas_per_sm, stages, prefetch_kb), "woq_tune_override")

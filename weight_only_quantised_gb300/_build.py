@@ -37,9 +37,10 @@ def needs_build() -> bool:
     return not os.path.exists(LIB) or os.path.getmtime(LIB) < _deps_mtime()
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(OUT_DIR, src + ".o")
+def _compile(src: str, verbose_ptxas: bool, out_dir: str = OUT_DIR, defines=()) -> str:
+    obj = os.path.join(out_dir, src + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden,-O2",
+           *[f"-D{d}" for d in defines],
            "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src), "-o", obj]
     if src.endswith(".cpp"):
         cmd[1:1] = ["-x", "cu"]
@@ -53,23 +54,27 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not needs_build():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, trace: bool = False) -> str:
+    """Build libwoq.so; trace=True builds libwoq_trace.so with per-CTA phase stamps instead."""
+    lib = os.path.join(PKG, "libwoq_trace.so") if trace else LIB
+    out_dir = os.path.join(OUT_DIR, "trace") if trace else OUT_DIR
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
+    defines = ("WOQ_TRACE",) if trace else ()
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    vs = os.path.join(OUT_DIR, "exports.map")
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, out_dir, defines), SOURCES))
+    vs = os.path.join(out_dir, "exports.map")
     with open(vs, "w") as f:
         f.write("{ global: woq_*; local: *; };\n")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, f"-Xlinker=--version-script={vs}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -4,7 +4,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/woq.h"
+#include "woq.h"
 #include "woq_gemv_launch.cuh"
 #include "woq_internal.h"
 #include "woq_layout.h"
@@ -18,6 +18,7 @@ std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_max_smem[kMaxDevices];
 std::atomic<int> g_override_cps{0};
 std::atomic<int> g_override_stages{0};
+std::atomic<int> g_override_prefetch_kb{-1};
 
 int current_device() {
   int d = 0;
@@ -52,17 +53,25 @@ int max_dynamic_smem() {
   return v;
 }
 
-// [barriers, flags: 256][reduction buffers][activations M x K int8][ring]
-static int red_bytes(int M) { return 2 * kConsumerWarps * M * kTileRows * 4; }
-static int act_offset(int M) { return 256 + red_bytes(M); }
-static int ring_offset(int M, int K) { return (int)align_up((size_t)act_offset(M) + (size_t)M * K, 128); }
-
-int smem_bytes_for(int bits, int M, int K, int stages) {
-  return ring_offset(M, K) + stages * kConsumerWarps * block_bytes(bits);
+// [barriers, flags, scratch: 512][reduction buffer][activations][ring]
+// activations: bf16 x quantised in place (fused, 2 M K bytes) or int8 q (M K bytes)
+static int red_bytes(int M) { return kStageBlocks * M * kTileRows * 4; }
+static constexpr int kMiscBytes = 512;
+static int act_offset(int M) { return kMiscBytes + red_bytes(M); }
+static int act_bytes(int M, int K, bool fused) { return (fused ? 2 : 1) * M * K; }
+static int ring_offset(int M, int K, bool fused) {
+  return (int)align_up((size_t)act_offset(M) + (size_t)act_bytes(M, K, fused), 128);
 }
 
-LaunchConfig choose_config(int bits, int M, int N, int K) {
-  LaunchConfig cfg = {0, 0, 0};
+int smem_bytes_for(int bits, int M, int K, bool fused, int stages) {
+  return ring_offset(M, K, fused) + stages * kStageBlocks * block_bytes(bits);
+}
+
+// Two CTAs (of this launch and the next) share an SM when each needs at most this much.
+static constexpr int kCoResidentBudget = (233472 - 2 * 1024) / 2;
+
+LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
+  LaunchConfig cfg = {0, 0, 0, 0};
   const int sms = sm_count();
   const int smem_max = max_dynamic_smem();
   if (sms <= 0 || smem_max <= 0) return cfg;
@@ -72,20 +81,32 @@ LaunchConfig choose_config(int bits, int M, int N, int K) {
   if (NB <= 0) return cfg;
   int cps = g_override_cps.load(std::memory_order_relaxed);
   if (cps <= 0) cps = 1;
-  // per-CTA shared memory budget: one CTA gets the opt-in maximum; two share the SM's 228 KB
-  const int budget = cps == 1 ? smem_max : (233472 - cps * 1024) / cps;
   int stages = g_override_stages.load(std::memory_order_relaxed);
-  if (stages <= 0) stages = 4;
-  while (stages >= 2 && smem_bytes_for(bits, M, K, stages) > budget) --stages;
+  if (stages > 0) {
+    const int budget = cps == 1 ? smem_max : kCoResidentBudget;
+    while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > budget) --stages;
+  } else {
+    // prefer a ring small enough for co-residency with the next launch, else the largest that fits
+    stages = 4;
+    while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > kCoResidentBudget) --stages;
+    if (stages < 2 && cps == 1) {
+      stages = 4;
+      while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > smem_max) --stages;
+    }
+  }
   if (stages < 2) return cfg;
-  // at least one stage (kConsumerWarps blocks) of work per CTA
+  const int stage_bytes = kStageBlocks * block_bytes(bits);
+  int pf_kb = g_override_prefetch_kb.load(std::memory_order_relaxed);
+  if (pf_kb < 0) pf_kb = 256;
+  // at least one stage (kStageBlocks blocks) of work per CTA
   long long ctas = (long long)sms * cps;
-  const long long by_work = (NB + kConsumerWarps - 1) / kConsumerWarps;
+  const long long by_work = (NB + kStageBlocks - 1) / kStageBlocks;
   if (ctas > by_work) ctas = by_work;
   if (ctas < 1) ctas = 1;
   cfg.ctas = (int)ctas;
   cfg.stages = stages;
-  cfg.smem_bytes = smem_bytes_for(bits, M, K, stages);
+  cfg.smem_bytes = smem_bytes_for(bits, M, K, fused, stages);
+  cfg.prefetch_stages = (int)(((long long)pf_kb * 1024 + stage_bytes - 1) / stage_bytes);
   return cfg;
 }
 
@@ -125,11 +146,23 @@ const char* woq_status_string(int status) {
   }
 }
 
-int woq_tune_override(int ctas_per_sm, int stages) {
-  if (ctas_per_sm < 0 || ctas_per_sm > 2 || stages < 0 || stages == 1 || stages > kMaxStages) return WOQ_ERR_SHAPE;
+int woq_tune_override(int ctas_per_sm, int stages, int prefetch_kb) {
+  if (ctas_per_sm < 0 || ctas_per_sm > 2 || stages < 0 || stages == 1 || stages > kMaxStages || prefetch_kb < -1 ||
+      prefetch_kb > 65536)
+    return WOQ_ERR_SHAPE;
   g_override_cps.store(ctas_per_sm);
   g_override_stages.store(stages);
+  g_override_prefetch_kb.store(prefetch_kb);
   return WOQ_OK;
+}
+
+int woq_max_k(int bits, int M, int fused) {
+  if ((bits != 4 && bits != 6) || M < 1 || M > kMaxM) return 0;
+  const int smem_max = max_dynamic_smem();
+  if (smem_max <= 0) return 0;
+  int K = (int)(kMaxMK / M) / kGroup * kGroup;
+  while (K > 0 && smem_bytes_for(bits, M, K, fused != 0, 2) > smem_max) K -= kGroup;
+  return K;
 }
 
 size_t woq_workspace_bytes(int bits, int M, int N, int K) {
@@ -196,7 +229,7 @@ static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_by
   if (!aligned(wpacked, 16) || !aligned(y, 4) || !aligned(ws, 16)) return WOQ_ERR_ALIGN;
   if (fused ? !aligned(x_bf16, 16) : (!aligned(q, 16) || !aligned(ascale, 4))) return WOQ_ERR_ALIGN;
   if (wpacked_bytes < packed_bytes(bits, N, K)) return WOQ_ERR_LAYOUT;
-  const LaunchConfig cfg = choose_config(bits, M, N, K);
+  const LaunchConfig cfg = choose_config(bits, M, N, K, fused);
   if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
   const WorkspaceLayout wl = workspace_layout(M, N, cfg.ctas);
   if (ws_bytes < wl.total || cfg.ctas > max_ctas_for_workspace()) return WOQ_ERR_WORKSPACE;
@@ -216,9 +249,10 @@ static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_by
   p.G = K / kGroup;
   p.NB = (long long)p.T * p.G;
   p.stages = cfg.stages;
+  p.prefetch_stages = cfg.prefetch_stages;
   p.act_offset = act_offset(M);
-  p.red_offset = 256;
-  p.ring_offset = ring_offset(M, K);
+  p.red_offset = kMiscBytes;
+  p.ring_offset = ring_offset(M, K, fused);
   const cudaError_t e = bits == 4 ? launch_gemv_w4(fused, M, p, cfg, stream) : launch_gemv_w6(fused, M, p, cfg, stream);
   return e == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
 }

@@ -80,6 +80,20 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Same without a cache policy (data that other kernels wrote and may read again).
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// Bring `bytes` of global memory into L2 ahead of use (no completion tracking).
+// src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: block until the grids this one depends on have
 // completed and their writes are visible (no-op when launched without the attribute).
 __device__ __forceinline__ void pdl_wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -105,6 +119,36 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t h16) {
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Activation quantisation: q = rne(x / s), where x / s is the IEEE round-to-nearest
+// quotient, for a row scale s = amax / 127 != 0 and rc = the correctly rounded
+// reciprocal of s.  t = fl(x * rc) is within |x/s| (3u + u^2) (u = 2^-24) of fl(x / s),
+// below 2.28e-5 since |x/s| <= 127 (1 + 2u).  Unless t lies within 3e-5 of a tie
+// (|t - rne(t)| > 0.5 - 3e-5), t and fl(x / s) round to the same integer; the caller
+// takes the IEEE division for the rare values that are that close (or when rc
+// overflowed).  |t| < 127.5, so no clamp to [-127, 127] is ever needed.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: t + magic rounds t to an integer (RNE)
+constexpr float kTieGuard = 0.5f - 3e-5f;
+
+// Low byte (two's complement) of rne(t) for |t| < 2^22, and whether t is near a tie.
+__device__ __forceinline__ uint32_t quant_byte_fast(float t, bool& near_tie) {
+  const float y = __fadd_rn(t, kRoundMagic);
+  const float r = __fsub_rn(y, kRoundMagic);
+  near_tie = !(fabsf(__fsub_rn(t, r)) <= kTieGuard);  // NaN (rc = inf) counts as near
+  return (uint32_t)__float_as_int(y) & 0xFFu;
+}
+
+// Low byte of rne(fl(x / s)) by the IEEE division (the slow, always-exact route).
+__device__ __forceinline__ uint32_t quant_byte_exact(float x, float s) {
+  return (uint32_t)(int)rintf(__fdiv_rn(x, s)) & 0xFFu;
+}
+
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 }  // namespace dev
 }  // namespace woq

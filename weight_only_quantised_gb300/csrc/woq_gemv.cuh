@@ -17,11 +17,15 @@
 //     the same number of bytes whatever N and K are.  A 128-row tile cut by a
 //     range boundary is finished by the last of its CTAs to arrive (partial sums
 //     in the workspace plus a ticket counter; no spin-waits, fixed summation
-//     order, so results are deterministic).
+//     order, so results are deterministic).  Each CTA works on its two cut tiles
+//     first, so the fix-up is off the launch's critical tail.
 //   * Warp 4 is the producer: one lane issues 1-D bulk copies (TMA engine) of
 //     whole stages (4 consecutive blocks of one tile, 33 KB for int4) into a
-//     ring of shared-memory stages, tracked by mbarriers, with an L2
-//     evict-first policy since every weight byte is read once.
+//     small ring of shared-memory stages tracked by mbarriers (L2 evict-first:
+//     every weight byte is read once), and keeps a window of later stages in
+//     flight from HBM into L2 with bulk L2 prefetches, so the bytes in flight do
+//     not depend on the ring's size.  The small ring lets the CTA of the next
+//     launch share the SM and start its weight stream before this one ends.
 //   * Warps 0..3 consume: warp w takes block w of each stage.  Lane l owns rows
 //     l, 32+l, 64+l, 96+l of the tile; for each 32-k quarter it reads its
 //     16-byte chunk per row (consecutive lanes, conflict-free) and the quarter's
@@ -29,14 +33,15 @@
 //     int6) to int8 lanes with two masks and a shift, and runs dp4a.  Per group
 //     the int32 dot is exact; the term (d * wscale) * ascale is formed with two
 //     fp32 roundings, as in the definition, and accumulated in fp32.
-//   * The activations (int8, M x K) sit in shared memory for the whole launch.
-//     The fused entry quantises bf16 x itself (amax pass + quantise pass over x,
-//     which is L2-resident), bit-identical to the standalone kernel.
-//   * Programmatic dependent launch: the producer starts streaming weights
-//     before the previous kernel in the stream has finished; consumers wait for
-//     it (griddepcontrol.wait) before reading activations or writing anything.
+//   * The activations arrive with one bulk copy and stay in shared memory for the
+//     whole launch.  The fused entry copies bf16 x, takes the per-row amax and
+//     quantises it in place, bit-identical to the standalone kernel.
+//   * Programmatic dependent launch: the producer streams weights before the
+//     previous kernel in the stream has finished; the activation copy, and every
+//     write to y or the workspace, wait for it (griddepcontrol.wait).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -56,18 +61,35 @@ struct GemvParams {
   float* partials;          // [ctas][2][M][128]
   int N, K, T, G;
   long long NB;             // T * G blocks
-  int stages;
+  int stages;               // shared-memory ring stages
+  int prefetch_stages;      // stages' worth of weights kept in flight into L2 beyond the ring
   int act_offset;           // shared-memory offsets (bytes)
   int red_offset;
   int ring_offset;
 };
 
+#ifdef WOQ_TRACE
+// Trace build only: per-CTA %globaltimer stamps of the launch phases (the last launch wins).
+constexpr int kTraceEvents = 16;
+constexpr int kTraceCtas = 1024;
+static __device__ unsigned long long g_trace[kTraceCtas * kTraceEvents];
+#define WOQ_TRACE_EV(ev)                                                               \
+  do {                                                                                 \
+    if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceEvents + (ev)] = dev::global_timer_ns(); \
+  } while (0)
+#else
+#define WOQ_TRACE_EV(ev) \
+  do {                   \
+  } while (0)
+#endif
+
 namespace kern {
 
-constexpr int kCW = 4;                 // consumer warps
-constexpr int kConsumers = kCW * 32;   // 128 = rows per tile
-constexpr int kSB = kCW;               // blocks per stage
+constexpr int kCW = 8;                 // consumer warps: two per block of a stage, 64 rows each
+constexpr int kConsumers = kCW * 32;   // 256
+constexpr int kSB = 4;                 // blocks per stage
 constexpr int kBarConsumers = 1;       // named barrier id for the consumer warps
+static_assert(kCW == 2 * kSB, "each block of a stage is split between two consumer warps");
 
 template <int BITS>
 struct Fmt {
@@ -94,26 +116,38 @@ __device__ __forceinline__ void unpack_word(uint32_t v, uint32_t uh, int e, uint
   }
 }
 
-// One block (128 rows x one group) by one warp: acc[j][m] += term(row 32j+lane, m).
+// One half block (rows 64h .. 64h+63 x one group) by one warp:
+// acc[jj][m] += term(row 32(2h+jj)+lane, m).  The int4 (or int6) lanes of the low and
+// high nibbles accumulate into separate int32 chains (more independent dp4a), summed
+// exactly at the end of the group.
 template <int BITS, int M>
-__device__ __forceinline__ void consume_block(const uint8_t* __restrict__ blk, const int8_t* __restrict__ act, int K,
-                                              int g, int lane, const float (&as)[M], float (&acc)[4][M]) {
+__device__ __forceinline__ void consume_half_block(const uint8_t* __restrict__ blk, const int8_t* __restrict__ act,
+                                                   int K, int g, int lane, int h, const float (&as)[M],
+                                                   float (&acc)[2][M]) {
   const uint2 sc = *reinterpret_cast<const uint2*>(blk + 8 * lane);
-  float wsc[4];
-  wsc[0] = dev::half_bits_to_float(sc.x & 0xFFFFu) * Fmt<BITS>::kDotScale;
-  wsc[1] = dev::half_bits_to_float(sc.x >> 16) * Fmt<BITS>::kDotScale;
-  wsc[2] = dev::half_bits_to_float(sc.y & 0xFFFFu) * Fmt<BITS>::kDotScale;
-  wsc[3] = dev::half_bits_to_float(sc.y >> 16) * Fmt<BITS>::kDotScale;
+  const uint32_t sw = h ? sc.y : sc.x;  // scales of rows 32(2h) + lane and 32(2h+1) + lane
+  float wsc[2];
+  wsc[0] = dev::half_bits_to_float(sw & 0xFFFFu) * Fmt<BITS>::kDotScale;
+  wsc[1] = dev::half_bits_to_float(sw >> 16) * Fmt<BITS>::kDotScale;
 
-  int dot[4][M];
+  int dlo[2][M], dhi[2][M];
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-    for (int m = 0; m < M; ++m) dot[j][m] = 0;
+    for (int m = 0; m < M; ++m) dlo[jj][m] = dhi[jj][m] = 0;
 
   const int8_t* ag = act + g * kGroup;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
+    uint4 v[2];
+    uint2 u[2] = {make_uint2(0u, 0u), make_uint2(0u, 0u)};
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int j = 2 * h + jj;
+      v[jj] = *reinterpret_cast<const uint4*>(blk + kScaleBytes + ((c * 4 + j) * 32 + lane) * 16);
+      if constexpr (BITS == 6)
+        u[jj] = *reinterpret_cast<const uint2*>(blk + kScaleBytes + kW4Bytes + ((c * 4 + j) * 32 + lane) * 8);
+    }
     uint32_t a[M][8];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
@@ -123,47 +157,195 @@ __device__ __forceinline__ void consume_block(const uint8_t* __restrict__ blk, c
       a[m][4] = a1.x; a[m][5] = a1.y; a[m][6] = a1.z; a[m][7] = a1.w;
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 v = *reinterpret_cast<const uint4*>(blk + kScaleBytes + ((c * 4 + j) * 32 + lane) * 16);
-      uint2 u = make_uint2(0u, 0u);
-      if constexpr (BITS == 6)
-        u = *reinterpret_cast<const uint2*>(blk + kScaleBytes + kW4Bytes + ((c * 4 + j) * 32 + lane) * 8);
-      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    for (int jj = 0; jj < 2; ++jj) {
+      const uint32_t vw[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         uint32_t lo, hi;
-        unpack_word<BITS>(vw[i], (i < 2) ? u.x : u.y, i & 1, lo, hi);
+        unpack_word<BITS>(vw[i], (i < 2) ? u[jj].x : u[jj].y, i & 1, lo, hi);
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          dot[j][m] = dev::dp4a_ss(lo, a[m][2 * i], dot[j][m]);
-          dot[j][m] = dev::dp4a_ss(hi, a[m][2 * i + 1], dot[j][m]);
+          dlo[jj][m] = dev::dp4a_ss(lo, a[m][2 * i], dlo[jj][m]);
+          dhi[jj][m] = dev::dp4a_ss(hi, a[m][2 * i + 1], dhi[jj][m]);
         }
       }
     }
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       // (d * wscale) * ascale with two fp32 roundings; lanes carry 16d (int4) or 4d (int6),
       // and wsc carries wscale / 16 (or / 4), so the first product is exactly fl(d * wscale)
-      const float t = __fmul_rn(__fmul_rn(dev::small_int_to_float(dot[j][m]), wsc[j]), as[m]);
-      acc[j][m] = __fadd_rn(acc[j][m], t);
+      const float t = __fmul_rn(__fmul_rn(dev::small_int_to_float(dlo[jj][m] + dhi[jj][m]), wsc[jj]), as[m]);
+      acc[jj][m] = __fadd_rn(acc[jj][m], t);
     }
 }
 
+// The blocks of one CTA's range, as work items (tile t, groups [ga, gb)) in processing
+// order: the partial tile at the start of the range, then the partial tile at its
+// end, then the whole tiles in between.  Split tiles are thereby finished early, and
+// the launch ends on tiles that need no fix-up.
+struct ItemOrder {
+  long long b_begin, b_end, first_tile, last_tile;
+  int G, n_items;
+  __device__ __forceinline__ ItemOrder(long long bb, long long be, int g) : b_begin(bb), b_end(be), G(g) {
+    first_tile = bb / g;
+    last_tile = (be - 1) / g;
+    n_items = (int)(last_tile - first_tile + 1);
+  }
+  __device__ __forceinline__ void get(int i, long long& t, int& ga, int& gb) const {
+    if (first_tile == last_tile) {
+      t = first_tile;
+      ga = (int)(b_begin - t * G);
+      gb = (int)(b_end - t * G);
+    } else if (i == 0) {
+      t = first_tile;
+      ga = (int)(b_begin - t * G);
+      gb = G;
+    } else if (i == 1) {
+      t = last_tile;
+      ga = 0;
+      gb = (int)(b_end - t * G);
+    } else {
+      t = first_tile + (i - 1);
+      ga = 0;
+      gb = G;
+    }
+  }
+};
+
+// Walks the ring stages (up to kSB consecutive blocks of one item) in processing order.
+struct StageCursor {
+  const ItemOrder* order;
+  int item;
+  long long t;
+  int ga, gb, g0;
+  __device__ __forceinline__ void start(const ItemOrder* o) {
+    order = o;
+    item = 0;
+    order->get(0, t, ga, gb);
+    g0 = ga;
+  }
+  __device__ __forceinline__ bool valid() const { return item < order->n_items; }
+  __device__ __forceinline__ int nb() const { return gb - g0 < kSB ? gb - g0 : kSB; }
+  __device__ __forceinline__ long long block() const { return t * order->G + g0; }
+  __device__ __forceinline__ void advance() {
+    g0 += kSB;
+    if (g0 >= gb) {
+      ++item;
+      if (item < order->n_items) {
+        order->get(item, t, ga, gb);
+        g0 = ga;
+      }
+    }
+  }
+};
+
+// Activation prologue of the fused entry, run by the consumer warps on the bf16 x
+// that one bulk copy placed at act[0, 2 M K): per-row amax, scale = amax / 127, and
+// q = rne(x / scale) written in place over the first M K bytes.  Rounds of
+// kConsumers * 32 values, read fully before any thread writes, walk the rows in
+// order: q byte e overwrites only x bytes of values already read.
+template <int M>
+__device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, int lane, int warp, float* s_scratch,
+                                                  float* s_as) {
+  const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
+  // amax: bf16 pairs, |.| by clearing sign bits, max of bf16 values is exact
+  float lmax[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    __nv_bfloat162 a4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a4[i] = __nv_bfloat162(__float2bfloat16_rn(0.0f), __float2bfloat16_rn(0.0f));
+    for (int e = tid * 8; e < K; e += kConsumers * 8) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xs + (size_t)m * K + e);
+      const uint32_t w4[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a4[i] = __hmax2(a4[i], *reinterpret_cast<const __nv_bfloat162*>(&w4[i]));
+    }
+    const __nv_bfloat162 a2 = __hmax2(__hmax2(a4[0], a4[1]), __hmax2(a4[2], a4[3]));
+    float a = fmaxf(__low2float(a2), __high2float(a2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    lmax[m] = a;
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int m = 0; m < M; ++m) s_scratch[warp * 4 + m] = lmax[m];
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    float amax = s_scratch[m];
+#pragma unroll
+    for (int w = 1; w < kCW; ++w) amax = fmaxf(amax, s_scratch[w * 4 + m]);
+    const float sc = __fdiv_rn(amax, 127.0f);
+    const float rc = __frcp_rn(sc);
+    if (tid == 0) s_as[m] = sc;
+    // this row's values, in rounds
+    for (int k0 = 0; k0 < K; k0 += kConsumers * 32) {
+      uint4 xv[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int k = k0 + 8 * (tid + kConsumers * v);
+        xv[v] = k < K ? *reinterpret_cast<const uint4*>(xs + (size_t)m * K + k) : make_uint4(0, 0, 0, 0);
+      }
+      dev::named_barrier_sync(kBarConsumers, kConsumers);
+      if (sc == 0.0f) {  // all-zero row: q = 0 (row-uniform branch)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int k = k0 + 8 * (tid + kConsumers * v);
+          if (k < K) *reinterpret_cast<uint2*>(act + (size_t)m * K + k) = make_uint2(0u, 0u);
+        }
+        continue;
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int k = k0 + 8 * (tid + kConsumers * v);
+        const uint32_t w4[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
+        float xf[8];
+        uint32_t qb[8];
+        bool near = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          xf[i] = __uint_as_float((i & 1) ? (w4[i >> 1] & 0xFFFF0000u) : (w4[i >> 1] << 16));
+          bool nt;
+          qb[i] = dev::quant_byte_fast(__fmul_rn(xf[i], rc), nt);
+          near |= nt;
+        }
+        // rare: a lane of the warp holds a quotient within 3e-5 of a tie; divide there
+        if (__any_sync(0xffffffffu, near && k < K)) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            bool nt;
+            dev::quant_byte_fast(__fmul_rn(xf[i], rc), nt);
+            if (nt) qb[i] = dev::quant_byte_exact(xf[i], sc);
+          }
+        }
+        if (k < K) {
+          const uint32_t lo = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
+          const uint32_t hi = qb[4] | (qb[5] << 8) | (qb[6] << 16) | (qb[7] << 24);
+          *reinterpret_cast<uint2*>(act + (size_t)m * K + k) = make_uint2(lo, hi);
+        }
+      }
+    }
+  }
+}
+
 template <int BITS, int M, bool FUSED>
-__global__ void __launch_bounds__(kConsumers + 32, 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvParams p) {
   constexpr int BB = Fmt<BITS>::kBlockBytes;
   constexpr int kStageBytes = kSB * BB;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + 8;
-  float* s_as = reinterpret_cast<float*>(smem + 128);
-  volatile int* s_flags = reinterpret_cast<volatile int*>(smem + 160);  // [0] ticket-last, [1] abort, [2] header-ok
-  float* s_scratch = reinterpret_cast<float*>(smem + 192);               // [4 warps] amax partials
-  int8_t* act = reinterpret_cast<int8_t*>(smem + p.act_offset);
-  float* red = reinterpret_cast<float*>(smem + p.red_offset);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);          // [8]
+  uint64_t* empty = full + 8;                                  // [8]
+  uint64_t* actbar = full + 16;                                // activations landed
+  volatile int* s_flags = reinterpret_cast<volatile int*>(smem + 136);  // [0] ticket-last, [1] abort, [2] header-ok
+  float* s_as = reinterpret_cast<float*>(smem + 160);          // [M] activation scales
+  float* s_scratch = reinterpret_cast<float*>(smem + 192);     // [8 warps][4 rows] amax partials, to byte 320
+  uint8_t* act = smem + p.act_offset;                          // bf16 x, quantised in place (fused) or int8 q
+  float* red = reinterpret_cast<float*>(smem + p.red_offset);  // [4 blocks][M][128 rows]
   uint8_t* ring = smem + p.ring_offset;
 
   const int tid = threadIdx.x;
@@ -175,46 +357,68 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) gemv_kernel(const GemvPara
   const long long b_end = range_begin(cta + 1, p.NB, C);
   const int G = p.G;
   const int stages = p.stages;
+  const ItemOrder order(b_begin, b_end, G);
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       dev::mbar_init(full + s, 1);
       dev::mbar_init(empty + s, kCW);
     }
+    dev::mbar_init(actbar, 1);
     s_flags[0] = 0;
     s_flags[1] = 0;
     s_flags[2] = 1;
     dev::fence_mbar_init();
   }
   __syncthreads();
+  if (tid == 0) WOQ_TRACE_EV(0);
   // every CTA of this grid is resident (one per SM), so the next grid may be scheduled now
   dev::pdl_launch_dependents();
 
   if (warp == kCW) {
     // ---------------------------------------------------------------- producer
+    // weights do not depend on the previous grid: no griddepcontrol.wait here
     if (lane == 0) {
       const uint64_t pol = dev::l2_evict_first_policy();
       const uint8_t* blocks = p.w + kHeaderBytes;
+      StageCursor ld, pf;
+      ld.start(&order);
       long long it = 0;
       bool ok = true;
-      for (long long b = b_begin; b < b_end && ok;) {
-        const long long t = b / G;
-        const int g0 = (int)(b - t * G);
-        const int gend = (int)((b_end < (t + 1) * G ? b_end : (t + 1) * G) - t * G);
-        const int nb = gend - g0 < kSB ? gend - g0 : kSB;
-        const int slot = (int)(it % stages);
-        if (it >= stages && !dev::mbar_wait_bounded(empty + slot, (uint32_t)((it / stages - 1) & 1))) {
+      for (; ld.valid() && it < stages; ld.advance(), ++it) {
+        const int slot = (int)it;
+        const uint32_t bytes = (uint32_t)(ld.nb() * BB);
+        dev::mbar_arrive_expect_tx(full + slot, bytes);
+        dev::bulk_copy_g2s(ring + (size_t)slot * kStageBytes, blocks + (size_t)ld.block() * BB, bytes, full + slot, pol);
+      }
+      WOQ_TRACE_EV(1);
+      // keep prefetch_stages stages beyond the ring in flight into L2
+      pf = ld;
+      for (int k = 0; k < p.prefetch_stages && pf.valid(); ++k, pf.advance())
+        dev::bulk_prefetch_l2(blocks + (size_t)pf.block() * BB, (uint32_t)(pf.nb() * BB));
+      int slot = 0;
+      uint32_t phase = 0;  // parity of the empty-barrier phase to wait for
+      for (; ld.valid(); ld.advance(), ++it) {
+        if (!dev::mbar_wait_bounded(empty + slot, phase)) {
           ok = false;
           break;
         }
-        const uint32_t bytes = (uint32_t)(nb * BB);
+        const uint32_t bytes = (uint32_t)(ld.nb() * BB);
         dev::mbar_arrive_expect_tx(full + slot, bytes);
-        dev::bulk_copy_g2s(ring + (size_t)slot * kStageBytes, blocks + (size_t)b * BB, bytes, full + slot, pol);
-        ++it;
-        b += nb;
+        dev::bulk_copy_g2s(ring + (size_t)slot * kStageBytes, blocks + (size_t)ld.block() * BB, bytes, full + slot, pol);
+        if (pf.valid()) {
+          dev::bulk_prefetch_l2(blocks + (size_t)pf.block() * BB, (uint32_t)(pf.nb() * BB));
+          pf.advance();
+        }
+        if (++slot == stages) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
+      WOQ_TRACE_EV(9);
       if (!ok) atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
       // no bulk copy may still be landing in this CTA's shared memory when it exits
+      dev::mbar_wait_bounded(actbar, 0);
       const long long first = it > stages ? it - stages : 0;
       for (long long i = first; i < it; ++i) dev::mbar_wait_bounded(full + (int)(i % stages), (uint32_t)((i / stages) & 1));
     }
@@ -222,139 +426,121 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) gemv_kernel(const GemvPara
   }
 
   // -------------------------------------------------------------------- consumers
+  // activations (and y, the workspace) belong to the previous grid until it has completed
   dev::pdl_wait_prior_grids();
-
+  uint4 hdr0 = make_uint4(0, 0, 0, 0), hdr1 = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
+    WOQ_TRACE_EV(3);
+    const uint32_t act_bytes = (uint32_t)(FUSED ? 2 * M * p.K : M * p.K);
+    dev::mbar_arrive_expect_tx(actbar, act_bytes);
+    dev::bulk_copy_g2s(act, FUSED ? static_cast<const void*>(p.x) : static_cast<const void*>(p.q), act_bytes, actbar);
+    hdr0 = *reinterpret_cast<const uint4*>(p.w);
+    hdr1 = *reinterpret_cast<const uint4*>(p.w + 16);
+  }
+  float ascale_in = 0.0f;
+  if (!FUSED && tid < M) ascale_in = p.ascale[tid];
+
+  bool aborted = false;
+  if (!dev::mbar_wait_bounded(actbar, 0)) {
+    aborted = true;
+    s_flags[1] = 1;
+    atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
+  }
+  if (tid == 0) {
+    WOQ_TRACE_EV(4);
     // the packed header must describe this call's (bits, N, K)
-    const uint4 h0 = *reinterpret_cast<const uint4*>(p.w);
-    const uint4 h1 = *reinterpret_cast<const uint4*>(p.w + 16);
-    const bool hok = h0.x == kMagic && h0.y == kLayoutVersion && h0.z == (uint32_t)BITS && h0.w == (uint32_t)kTileRows &&
-                     h1.x == (uint32_t)p.N && h1.y == (uint32_t)p.K;
+    const bool hok = hdr0.x == kMagic && hdr0.y == kLayoutVersion && hdr0.z == (uint32_t)BITS &&
+                     hdr0.w == (uint32_t)kTileRows && hdr1.x == (uint32_t)p.N && hdr1.y == (uint32_t)p.K;
     if (!hok) {
       s_flags[2] = 0;
       atomicOr(p.status, 0x1u /* WOQ_DEVERR_HEADER */);
     }
   }
-
-  // activations -> shared memory (int8, [M][K])
   if constexpr (FUSED) {
-    // pass 1: amax per row; pass 2: q = rne(x / (amax / 127)), as the standalone kernel
-#pragma unroll 1
-    for (int m = 0; m < M; ++m) {
-      const uint16_t* xr = p.x + (size_t)m * p.K;
-      float amax = 0.0f;
-      for (int e = tid * 8; e < p.K; e += kConsumers * 8) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + e));
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          amax = fmaxf(amax, fabsf(dev::bf16_bits_to_float(w4[i] & 0xFFFFu)));
-          amax = fmaxf(amax, fabsf(dev::bf16_bits_to_float(w4[i] >> 16)));
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      if (lane == 0) s_scratch[warp] = amax;
-      dev::named_barrier_sync(kBarConsumers, kConsumers);
-      amax = fmaxf(fmaxf(s_scratch[0], s_scratch[1]), fmaxf(s_scratch[2], s_scratch[3]));
-      const float s = __fdiv_rn(amax, 127.0f);
-      dev::named_barrier_sync(kBarConsumers, kConsumers);  // s_scratch is reused by the next row
-      if (tid == 0) s_as[m] = s;
-      for (int e = tid * 8; e < p.K; e += kConsumers * 8) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + e));
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-        uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t bits16 = (i & 1) ? (w4[i >> 1] >> 16) : (w4[i >> 1] & 0xFFFFu);
-          int qi = 0;
-          if (s != 0.0f) {
-            const float r = rintf(__fdiv_rn(dev::bf16_bits_to_float(bits16), s));
-            qi = (int)fminf(fmaxf(r, -127.0f), 127.0f);
-          }
-          packed[i >> 2] |= ((uint32_t)qi & 0xFFu) << (8 * (i & 3));
-        }
-        *reinterpret_cast<uint2*>(act + (size_t)m * p.K + e) = make_uint2(packed[0], packed[1]);
-      }
-    }
+    quantise_prologue<M>(act, p.K, tid, lane, warp, s_scratch, s_as);
   } else {
-    const int mk16 = (M * p.K) >> 4;
-    for (int i = tid; i < mk16; i += kConsumers)
-      reinterpret_cast<uint4*>(act)[i] = __ldg(reinterpret_cast<const uint4*>(p.q) + i);
-    if (tid < M) s_as[tid] = p.ascale[tid];
+    if (tid < M) s_as[tid] = ascale_in;
   }
   dev::named_barrier_sync(kBarConsumers, kConsumers);
+  if (tid == 0) WOQ_TRACE_EV(6);
 
+  const int8_t* actq = reinterpret_cast<const int8_t*>(act);
   float as[M];
 #pragma unroll
   for (int m = 0; m < M; ++m) as[m] = s_as[m];
   const bool header_ok = s_flags[2] != 0;
+  const int hb = warp >> 1;  // block of the stage this warp works on
+  const int hh = warp & 1;   // its row half
 
-  const long long first_tile = b_begin / G;
-  long long it = 0;
-  int buf = 0;
-  bool aborted = false;
-  for (long long b = b_begin; b < b_end;) {
-    const long long t = b / G;
-    const int ga = (int)(b - t * G);
-    const long long item_end = b_end < (t + 1) * G ? b_end : (t + 1) * G;
-    const int gb = (int)(item_end - t * G);
+  int slot = 0;
+  uint32_t phase = 0;  // parity of the full-barrier phase to wait for
+  bool first_stage = true;
+  for (int item = 0; item < order.n_items; ++item) {
+    long long t;
+    int ga, gb;
+    order.get(item, t, ga, gb);
 
-    float acc[4][M];
+    float acc[2][M];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[j][m] = 0.0f;
+      for (int m = 0; m < M; ++m) acc[jj][m] = 0.0f;
 
     for (int g0 = ga; g0 < gb; g0 += kSB) {
       const int nb = gb - g0 < kSB ? gb - g0 : kSB;
-      const int slot = (int)(it % stages);
-      if (!aborted && !dev::mbar_wait_bounded(full + slot, (uint32_t)((it / stages) & 1))) {
+      if (!aborted && !dev::mbar_wait_bounded(full + slot, phase)) {
         aborted = true;
         s_flags[1] = 1;
         atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
       }
-      if (!aborted && warp < nb)
-        consume_block<BITS, M>(ring + (size_t)slot * kStageBytes + (size_t)warp * BB, act, p.K, g0 + warp, lane, as,
-                               acc);
+      if (tid == 0 && first_stage) WOQ_TRACE_EV(7);
+      first_stage = false;
+      if (!aborted && hb < nb)
+        consume_half_block<BITS, M>(ring + (size_t)slot * kStageBytes + (size_t)hb * BB, actq, p.K, g0 + hb, lane, hh,
+                                    as, acc);
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(empty + slot);
-      ++it;
+      if (++slot == stages) {
+        slot = 0;
+        phase ^= 1u;
+      }
     }
 
-    // reduce the four warps' partial sums for this tile: red[buf][warp][m][row]
-    float* rb = red + (size_t)buf * (kCW * M * kTileRows);
+    // reduce the four blocks' partial sums for this tile: red[block][m][row]
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-      for (int m = 0; m < M; ++m) rb[(warp * M + m) * kTileRows + 32 * j + lane] = acc[j][m];
+      for (int m = 0; m < M; ++m) red[(hb * M + m) * kTileRows + 64 * hh + 32 * jj + lane] = acc[jj][m];
     dev::named_barrier_sync(kBarConsumers, kConsumers);
     const bool write_ok = header_ok && s_flags[1] == 0;
-    const int row = tid;
+    const int row = tid & (kTileRows - 1);
+    const bool row_thread = tid < kTileRows;
     const long long n = t * kTileRows + row;
     float sum[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      float s = rb[(0 * M + m) * kTileRows + row];
+      float s = red[(0 * M + m) * kTileRows + row];
 #pragma unroll
-      for (int w = 1; w < kCW; ++w) s = __fadd_rn(s, rb[(w * M + m) * kTileRows + row]);
+      for (int b = 1; b < kSB; ++b) s = __fadd_rn(s, red[(b * M + m) * kTileRows + row]);
       sum[m] = s;
     }
+    dev::named_barrier_sync(kBarConsumers, kConsumers);  // red may be rewritten from here on
+    if (tid == 0 && item == 0) WOQ_TRACE_EV(10);
+    if (tid == 0 && item == 1) WOQ_TRACE_EV(11);
     if (ga == 0 && gb == G) {
-      if (write_ok && n < p.N) {
+      if (write_ok && row_thread && n < p.N) {
 #pragma unroll
         for (int m = 0; m < M; ++m) p.y[(size_t)m * p.N + n] = sum[m];
       }
     } else {
-      // tile split across CTAs: publish this CTA's part; the last to arrive sums all parts in CTA order.
-      // Every consumer thread takes both barriers whatever write_ok says (no divergent bar.sync).
-      const int part = (t == first_tile) ? 0 : 1;
+      // tile split across CTAs: publish this CTA's part; the last to arrive sums all parts
+      // in CTA order.  Every consumer thread takes both barriers (no divergent bar.sync).
+      const int part = (t == order.first_tile) ? 0 : 1;
       float* mine = p.partials + ((size_t)(cta * 2 + part) * M) * kTileRows;
-      if (write_ok) {
+      if (write_ok && row_thread) {
 #pragma unroll
         for (int m = 0; m < M; ++m) mine[m * kTileRows + row] = sum[m];
       }
-      __threadfence();
       dev::named_barrier_sync(kBarConsumers, kConsumers);
       if (tid == 0) {
         int last = 0;
@@ -362,15 +548,15 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) gemv_kernel(const GemvPara
           const long long c_first = cta_of_block(t * G, p.NB, C);
           const long long c_last = cta_of_block(t * G + G - 1, p.NB, C);
           const unsigned parts = (unsigned)(c_last - c_first + 1);
-          const unsigned prev = atomicAdd(p.tickets + t, 1u);
+          // release this CTA's partials (ordered before by the barrier), acquire the others'
+          const unsigned prev = dev::atomic_add_acq_rel_gpu(p.tickets + t, 1u);
           last = prev == parts - 1;
           if (last) p.tickets[t] = 0u;  // ready for the next launch
         }
         s_flags[0] = last;
       }
       dev::named_barrier_sync(kBarConsumers, kConsumers);
-      if (s_flags[0]) {
-        __threadfence();
+      if (s_flags[0] && row_thread) {
         const long long c_first = cta_of_block(t * G, p.NB, C);
         const long long c_last = cta_of_block(t * G + G - 1, p.NB, C);
         float tot[M];
@@ -388,9 +574,8 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) gemv_kernel(const GemvPara
         }
       }
     }
-    buf ^= 1;
-    b = item_end;
   }
+  if (tid == 0) WOQ_TRACE_EV(8);
 }
 
 }  // namespace kern

@@ -13,9 +13,10 @@ bool header_matches(const void* src, int bits, int N, int K);
 
 // Launch configuration of one GEMV / linear launch (chosen by the launch table).
 struct LaunchConfig {
-  int ctas;         // grid size (CTAs); each CTA streams an equal share of the blocks
-  int stages;       // ring stages of kConsumerWarps blocks each
-  int smem_bytes;   // dynamic shared memory per CTA
+  int ctas;             // grid size (CTAs); each CTA streams an equal share of the blocks
+  int stages;           // ring stages of kStageBlocks blocks each
+  int smem_bytes;       // dynamic shared memory per CTA
+  int prefetch_stages;  // stages kept in flight into L2 beyond the ring
 };
 
 // Workspace layout: [status word + pad: 256 B][tickets: uint32 per tile, padded to 256 B][partials]
@@ -25,14 +26,15 @@ struct WorkspaceLayout {
   size_t total;
 };
 
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kStageBlocks = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 8;
 
 int sm_count();                       // SMs of the current device (cached per device)
 int max_dynamic_smem();               // opt-in shared memory per block of the current device
-int smem_bytes_for(int bits, int M, int K, int stages);
-LaunchConfig choose_config(int bits, int M, int N, int K);
+int smem_bytes_for(int bits, int M, int K, bool fused, int stages);
+LaunchConfig choose_config(int bits, int M, int N, int K, bool fused);
 WorkspaceLayout workspace_layout(int M, int N, int ctas);
 
 // Kernel launchers (woq_gemv.cu); return a cudaError_t.

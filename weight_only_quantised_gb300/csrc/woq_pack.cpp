@@ -6,7 +6,7 @@
 // defined in woq_layout.h; this file only moves nibbles and half-words.
 #include <string.h>
 
-#include "../../include/woq.h"
+#include "woq.h"
 #include "woq_internal.h"
 #include "woq_layout.h"
 
