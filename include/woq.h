@@ -126,12 +126,13 @@ WOQ_API int woq_pack_device(int bits, const uint8_t* q_dev, const uint16_t* scal
 
 /* ---------------------------------------------------------------------------
  * Workspace.  GEMV / linear launches split the weight stream evenly over the
- * GPU's SMs; a 128-row tile that straddles two CTAs is finished by the last
- * CTA to reach it, through partial sums and a ticket counter in the workspace.
- * The workspace (device, caller-owned) must be zero-filled once before first
- * use (woq_workspace_init); every launch leaves its counters at zero again.
- * One workspace must not be used by two launches that can run at the same time.
- * Its size depends on the current device's SM count.
+ * GPU's SMs; a 128-row tile that straddles CTAs is finished by one of them,
+ * which sums the others' partial results (tagged words in the workspace) in a
+ * fixed order.  The workspace (device, caller-owned) must be zero-filled once
+ * before first use (woq_workspace_init); every successful launch leaves it zero
+ * again (after a WOQ_DEVERR_TIMEOUT, zero-fill it again).  One workspace must
+ * not be used by two launches that can run at the same time.  Its size depends
+ * on the current device's SM count.
  * --------------------------------------------------------------------------- */
 
 /* Bytes of workspace a GEMV / linear launch of this shape needs on the current device (0 if invalid). */

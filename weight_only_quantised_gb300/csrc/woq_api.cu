@@ -19,6 +19,7 @@ std::atomic<int> g_max_smem[kMaxDevices];
 std::atomic<int> g_override_cps{0};
 std::atomic<int> g_override_stages{0};
 std::atomic<int> g_override_prefetch_kb{-1};
+std::atomic<int> g_launch_counter{0};  // numbers GEMV launches (trace builds key their stamps by it)
 
 int current_device() {
   int d = 0;
@@ -111,11 +112,10 @@ LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
 }
 
 WorkspaceLayout workspace_layout(int M, int N, int ctas) {
+  (void)N;
   WorkspaceLayout wl;
-  const size_t T = (size_t)(N + kTileRows - 1) / kTileRows;
-  wl.tickets_offset = 256;
-  wl.partials_offset = align_up(wl.tickets_offset + T * 4, 256);
-  wl.total = wl.partials_offset + (size_t)ctas * 2 * (size_t)M * kTileRows * 4;
+  wl.parts_offset = 256;
+  wl.total = wl.parts_offset + (size_t)ctas * 2 * (size_t)M * kTileRows * 8;
   return wl;
 }
 
@@ -241,18 +241,20 @@ static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_by
   p.y = y;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<uint32_t*>(wsb);
-  p.tickets = reinterpret_cast<uint32_t*>(wsb + wl.tickets_offset);
-  p.partials = reinterpret_cast<float*>(wsb + wl.partials_offset);
+  p.parts = reinterpret_cast<unsigned long long*>(wsb + wl.parts_offset);
   p.N = N;
   p.K = K;
   p.T = (N + kTileRows - 1) / kTileRows;
   p.G = K / kGroup;
-  p.NB = (long long)p.T * p.G;
+  const unsigned long long nb64 = (unsigned long long)p.T * (unsigned long long)p.G;
+  if ((nb64 + 1) * (unsigned long long)(cfg.ctas + 1) >= (1ull << 32)) return WOQ_ERR_SHAPE;  // 32-bit partition math
+  p.NB = (uint32_t)nb64;
   p.stages = cfg.stages;
   p.prefetch_stages = cfg.prefetch_stages;
   p.act_offset = act_offset(M);
   p.red_offset = kMiscBytes;
   p.ring_offset = ring_offset(M, K, fused);
+  p.launch_id = g_launch_counter.fetch_add(1, std::memory_order_relaxed) & 0x7fffffff;
   const cudaError_t e = bits == 4 ? launch_gemv_w4(fused, M, p, cfg, stream) : launch_gemv_w6(fused, M, p, cfg, stream);
   return e == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
 }
@@ -289,5 +291,12 @@ int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_bytes, co
   return launch_group_dots(bits, wpacked, q, M, N, K, dots, (cudaStream_t)stream) == cudaSuccess ? WOQ_OK
                                                                                                   : WOQ_ERR_CUDA;
 }
+
+#ifdef WOQ_TRACE
+// Trace build only: the id the next GEMV / linear launch will get.
+__attribute__((visibility("default"))) int woq_trace_next_launch_id(void) {
+  return g_launch_counter.load() & 0x7fffffff;
+}
+#endif
 
 }  // extern "C"

@@ -143,6 +143,16 @@ __device__ __forceinline__ uint32_t quant_byte_exact(float x, float s) {
   return (uint32_t)(int)rintf(__fdiv_rn(x, s)) & 0xFFu;
 }
 
+// 64-bit relaxed global load / store at GPU scope (single-copy atomic for aligned words).
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Atomic add with acquire-release semantics at GPU scope; returns the old value.
 __device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
   uint32_t old;

@@ -57,25 +57,28 @@ struct GemvParams {
   const float* ascale;      // fp32 [M] (int8 entry)
   float* y;                 // fp32 [M][N]
   uint32_t* status;         // workspace status word
-  uint32_t* tickets;        // one counter per tile
-  float* partials;          // [ctas][2][M][128]
+  unsigned long long* parts;  // [ctas][2][M][128] tagged partial sums of split tiles (tag << 32 | fp32 bits)
   int N, K, T, G;
-  long long NB;             // T * G blocks
+  uint32_t NB;              // T * G blocks; (grid + 1) * NB < 2^32, so partition math stays 32-bit
   int stages;               // shared-memory ring stages
   int prefetch_stages;      // stages' worth of weights kept in flight into L2 beyond the ring
   int act_offset;           // shared-memory offsets (bytes)
   int red_offset;
   int ring_offset;
+  int launch_id;            // trace builds only: which trace slot this launch writes
 };
 
 #ifdef WOQ_TRACE
-// Trace build only: per-CTA %globaltimer stamps of the launch phases (the last launch wins).
+// Trace build only: %globaltimer stamps per (launch slot, CTA, event); no atomics.
+constexpr int kTraceSlots = 16;
+constexpr int kTraceCtas = 512;
 constexpr int kTraceEvents = 16;
-constexpr int kTraceCtas = 1024;
-static __device__ unsigned long long g_trace[kTraceCtas * kTraceEvents];
-#define WOQ_TRACE_EV(ev)                                                               \
-  do {                                                                                 \
-    if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceEvents + (ev)] = dev::global_timer_ns(); \
+static __device__ unsigned long long g_trace[kTraceSlots * kTraceCtas * kTraceEvents];
+#define WOQ_TRACE_EV(ev)                                                                              \
+  do {                                                                                                \
+    if (blockIdx.x < kTraceCtas)                                                                      \
+      g_trace[((p.launch_id % kTraceSlots) * kTraceCtas + blockIdx.x) * kTraceEvents + (ev)] =        \
+          dev::global_timer_ns();                                                                     \
   } while (0)
 #else
 #define WOQ_TRACE_EV(ev) \
@@ -97,11 +100,34 @@ struct Fmt {
   static constexpr float kDotScale = BITS == 4 ? 0.0625f : 0.25f;  // lanes hold 16w (int4) or 4w (int6)
 };
 
-// first block of CTA c under an even split of NB blocks over C CTAs
-__device__ __forceinline__ long long range_begin(long long c, long long NB, long long C) { return c * NB / C; }
+// first block of CTA c under an even split of NB blocks over C CTAs ((C + 1) * NB < 2^32)
+__device__ __forceinline__ uint32_t range_begin(uint32_t c, uint32_t NB, uint32_t C) { return c * NB / C; }
 // CTA whose range holds block b
-__device__ __forceinline__ long long cta_of_block(long long b, long long NB, long long C) {
-  return ((b + 1) * C - 1) / NB;
+__device__ __forceinline__ uint32_t cta_of_block(uint32_t b, uint32_t NB, uint32_t C) { return ((b + 1) * C - 1) / NB; }
+
+// Expected finish time, in blocks streamed, of CTA c's part of tile t, for a tile that
+// CTA c shares (its first or last tile) under the processing order of ItemOrder.
+__device__ __forceinline__ uint32_t part_finish(uint32_t c, uint32_t t, uint32_t NB, uint32_t C, uint32_t G) {
+  const uint32_t bb = range_begin(c, NB, C), be = range_begin(c + 1, NB, C);
+  const uint32_t ft = bb / G, lt = (be - 1) / G;
+  if (ft == lt) return be - bb;
+  const uint32_t a = (ft + 1) * G - bb;   // the start item, processed first
+  return t == ft ? a : a + (be - lt * G);  // the end item, processed second
+}
+
+// Whether this CTA combines split tile t: its part is expected to finish last (ties:
+// the lowest CTA).  Every CTA sharing the tile reaches the same answer.
+__device__ __forceinline__ bool is_combiner(uint32_t cta, uint32_t t, uint32_t NB, uint32_t C, uint32_t G) {
+  const uint32_t c_first = cta_of_block(t * G, NB, C), c_last = cta_of_block(t * G + G - 1, NB, C);
+  uint32_t comb = c_first, best = 0;
+  for (uint32_t c2 = c_first; c2 <= c_last; ++c2) {
+    const uint32_t f = part_finish(c2, t, NB, C, G);
+    if (c2 == c_first || f > best) {
+      best = f;
+      comb = c2;
+    }
+  }
+  return comb == cta;
 }
 
 // int4 / int6 lanes of word i of a 16-byte chunk: lo covers k0..k0+3, hi k0+4..k0+7
@@ -187,14 +213,14 @@ __device__ __forceinline__ void consume_half_block(const uint8_t* __restrict__ b
 // end, then the whole tiles in between.  Split tiles are thereby finished early, and
 // the launch ends on tiles that need no fix-up.
 struct ItemOrder {
-  long long b_begin, b_end, first_tile, last_tile;
+  uint32_t b_begin, b_end, first_tile, last_tile;
   int G, n_items;
-  __device__ __forceinline__ ItemOrder(long long bb, long long be, int g) : b_begin(bb), b_end(be), G(g) {
-    first_tile = bb / g;
-    last_tile = (be - 1) / g;
+  __device__ __forceinline__ ItemOrder(uint32_t bb, uint32_t be, int g) : b_begin(bb), b_end(be), G(g) {
+    first_tile = bb / (uint32_t)g;
+    last_tile = (be - 1) / (uint32_t)g;
     n_items = (int)(last_tile - first_tile + 1);
   }
-  __device__ __forceinline__ void get(int i, long long& t, int& ga, int& gb) const {
+  __device__ __forceinline__ void get(int i, uint32_t& t, int& ga, int& gb) const {
     if (first_tile == last_tile) {
       t = first_tile;
       ga = (int)(b_begin - t * G);
@@ -219,7 +245,7 @@ struct ItemOrder {
 struct StageCursor {
   const ItemOrder* order;
   int item;
-  long long t;
+  uint32_t t;
   int ga, gb, g0;
   __device__ __forceinline__ void start(const ItemOrder* o) {
     order = o;
@@ -229,7 +255,7 @@ struct StageCursor {
   }
   __device__ __forceinline__ bool valid() const { return item < order->n_items; }
   __device__ __forceinline__ int nb() const { return gb - g0 < kSB ? gb - g0 : kSB; }
-  __device__ __forceinline__ long long block() const { return t * order->G + g0; }
+  __device__ __forceinline__ uint32_t block() const { return t * (uint32_t)order->G + (uint32_t)g0; }
   __device__ __forceinline__ void advance() {
     g0 += kSB;
     if (g0 >= gb) {
@@ -351,10 +377,10 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const long long C = gridDim.x;
-  const long long cta = blockIdx.x;
-  const long long b_begin = range_begin(cta, p.NB, C);
-  const long long b_end = range_begin(cta + 1, p.NB, C);
+  const uint32_t C = gridDim.x;
+  const uint32_t cta = blockIdx.x;
+  const uint32_t b_begin = range_begin(cta, p.NB, C);
+  const uint32_t b_end = range_begin(cta + 1, p.NB, C);
   const int G = p.G;
   const int stages = p.stages;
   const ItemOrder order(b_begin, b_end, G);
@@ -426,6 +452,19 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
   }
 
   // -------------------------------------------------------------------- consumers
+  // roles in the split tiles (only the first two items can be split), worked out while the
+  // previous grid may still be running
+  bool comb0 = false, comb1 = false;
+  {
+    uint32_t t;
+    int ga, gb;
+    order.get(0, t, ga, gb);
+    if (!(ga == 0 && gb == G)) comb0 = is_combiner(cta, t, p.NB, C, (uint32_t)G);
+    if (order.n_items > 1) {
+      order.get(1, t, ga, gb);
+      if (!(ga == 0 && gb == G)) comb1 = is_combiner(cta, t, p.NB, C, (uint32_t)G);
+    }
+  }
   // activations (and y, the workspace) belong to the previous grid until it has completed
   dev::pdl_wait_prior_grids();
   uint4 hdr0 = make_uint4(0, 0, 0, 0), hdr1 = make_uint4(0, 0, 0, 0);
@@ -476,7 +515,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
   uint32_t phase = 0;  // parity of the full-barrier phase to wait for
   bool first_stage = true;
   for (int item = 0; item < order.n_items; ++item) {
-    long long t;
+    uint32_t t;
     int ga, gb;
     order.get(item, t, ga, gb);
 
@@ -515,7 +554,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
     const bool write_ok = header_ok && s_flags[1] == 0;
     const int row = tid & (kTileRows - 1);
     const bool row_thread = tid < kTileRows;
-    const long long n = t * kTileRows + row;
+    const uint32_t n = t * kTileRows + row;
     float sum[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
@@ -533,44 +572,58 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
         for (int m = 0; m < M; ++m) p.y[(size_t)m * p.N + n] = sum[m];
       }
     } else {
-      // tile split across CTAs: publish this CTA's part; the last to arrive sums all parts
-      // in CTA order.  Every consumer thread takes both barriers (no divergent bar.sync).
-      const int part = (t == order.first_tile) ? 0 : 1;
-      float* mine = p.partials + ((size_t)(cta * 2 + part) * M) * kTileRows;
-      if (write_ok && row_thread) {
+      // Tile split across CTAs.  The part expected to finish last (its CTA is the
+      // "combiner") sums all parts in CTA order and writes y; every other CTA publishes its
+      // part as tagged 64-bit words (value and tag land in one store, so a reader that sees
+      // the tag sees the value) and moves on.  No atomics, no barrier: the combiner polls
+      // (bounded) and clears the words for the next launch.
+      if (row_thread) {
+        const uint32_t c_first = cta_of_block(t * G, p.NB, C);
+        const uint32_t c_last = cta_of_block(t * G + G - 1, p.NB, C);
+        const bool comb = item == 0 ? comb0 : comb1;
+        if (!comb) {
+          if (write_ok) {
+            const int part = (t == order.first_tile) ? 0 : 1;
+            unsigned long long* mine = p.parts + ((size_t)(cta * 2 + part) * M) * kTileRows;
 #pragma unroll
-        for (int m = 0; m < M; ++m) mine[m * kTileRows + row] = sum[m];
-      }
-      dev::named_barrier_sync(kBarConsumers, kConsumers);
-      if (tid == 0) {
-        int last = 0;
-        if (write_ok) {
-          const long long c_first = cta_of_block(t * G, p.NB, C);
-          const long long c_last = cta_of_block(t * G + G - 1, p.NB, C);
-          const unsigned parts = (unsigned)(c_last - c_first + 1);
-          // release this CTA's partials (ordered before by the barrier), acquire the others'
-          const unsigned prev = dev::atomic_add_acq_rel_gpu(p.tickets + t, 1u);
-          last = prev == parts - 1;
-          if (last) p.tickets[t] = 0u;  // ready for the next launch
-        }
-        s_flags[0] = last;
-      }
-      dev::named_barrier_sync(kBarConsumers, kConsumers);
-      if (s_flags[0] && row_thread) {
-        const long long c_first = cta_of_block(t * G, p.NB, C);
-        const long long c_last = cta_of_block(t * G + G - 1, p.NB, C);
-        float tot[M];
+            for (int m = 0; m < M; ++m)
+              dev::st_relaxed_u64(mine + m * kTileRows + row, (1ull << 32) | __float_as_uint(sum[m]));
+          }
+        } else if (write_ok) {
+          float tot[M];
 #pragma unroll
-        for (int m = 0; m < M; ++m) tot[m] = 0.0f;
-        for (long long c2 = c_first; c2 <= c_last; ++c2) {
-          const int part2 = (t == range_begin(c2, p.NB, C) / G) ? 0 : 1;
-          const float* src = p.partials + ((size_t)(c2 * 2 + part2) * M) * kTileRows;
+          for (int m = 0; m < M; ++m) tot[m] = 0.0f;
+          bool ok = true;
+          for (uint32_t c2 = c_first; c2 <= c_last; ++c2) {
+            if (c2 == cta) {
 #pragma unroll
-          for (int m = 0; m < M; ++m) tot[m] = __fadd_rn(tot[m], __ldcg(src + m * kTileRows + row));
-        }
-        if (n < p.N) {
+              for (int m = 0; m < M; ++m) tot[m] = __fadd_rn(tot[m], sum[m]);
+              continue;
+            }
+            const int part2 = (t == range_begin(c2, p.NB, C) / (uint32_t)G) ? 0 : 1;
+            unsigned long long* src = p.parts + ((size_t)(c2 * 2 + part2) * M) * kTileRows;
 #pragma unroll
-          for (int m = 0; m < M; ++m) p.y[(size_t)m * p.N + n] = tot[m];
+            for (int m = 0; m < M; ++m) {
+              unsigned long long w = dev::ld_relaxed_u64(src + m * kTileRows + row);
+              if (!(w >> 32)) {
+                const uint64_t t0 = dev::global_timer_ns();
+                while (!(w >> 32)) {
+                  if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) break;
+                  __nanosleep(100);
+                  w = dev::ld_relaxed_u64(src + m * kTileRows + row);
+                }
+              }
+              if (!(w >> 32)) ok = false;
+              tot[m] = __fadd_rn(tot[m], __uint_as_float((uint32_t)w));
+              dev::st_relaxed_u64(src + m * kTileRows + row, 0ull);  // ready for the next launch
+            }
+          }
+          if (!ok) {
+            atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
+          } else if (n < p.N) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) p.y[(size_t)m * p.N + n] = tot[m];
+          }
         }
       }
     }

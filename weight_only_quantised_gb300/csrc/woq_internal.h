@@ -19,10 +19,9 @@ struct LaunchConfig {
   int prefetch_stages;  // stages kept in flight into L2 beyond the ring
 };
 
-// Workspace layout: [status word + pad: 256 B][tickets: uint32 per tile, padded to 256 B][partials]
+// Workspace layout: [status word + pad: 256 B][tagged partial sums: ctas x 2 x M x 128 x 8 B]
 struct WorkspaceLayout {
-  size_t tickets_offset;
-  size_t partials_offset;
+  size_t parts_offset;
   size_t total;
 };
 
