@@ -46,6 +46,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-div", type=int, default=8, help="oracle sample: 1/div of every linear's rows")
+    ap.add_argument("--linear", default="", help="time one 27B-class linear (qkv, o, gate_up, down, lm_head) "
+                                                 "instead of the step: a graph of launches over distinct weight copies")
+    ap.add_argument("--int8", action="store_true", help="with --linear: the int8 entry (act_quant once, then GEMV)")
     return ap.parse_args()
 
 
@@ -431,8 +434,71 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_linear(args):
+    """One linear of the 27B-class step, launched back to back over enough distinct packed
+    copies that their total exceeds 1 GB (every launch streams its weights from HBM)."""
+    import torch
+
+    import synthetic
+    import weight_only_quantised_gb300 as woq
+    shapes = dict(synthetic.LINEARS_27B)
+    shapes["lm_head"] = synthetic.LM_HEAD_27B
+    K, N = shapes[args.linear]
+    M = args.m
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pb = woq.woq_packed_bytes(4, N, K)
+    copies = max(4, int(1.2e9 // pb))
+    w, s = synthetic.weights(4, N, K, synthetic.sub_seed(2, args.linear), device=dev)
+    bufs = []
+    for _ in range(copies):
+        p = torch.empty(pb, dtype=torch.uint8, device=dev)
+        woq.woq_pack_device(4, w, s.view(torch.int16), N, K, p)
+        bufs.append(p)
+    del w, s
+    x = synthetic.activations(M, K, synthetic.sub_seed(2, "x", M, K), device=dev)
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    a = torch.empty((M,), dtype=torch.float32, device=dev)
+    woq.woq_act_quant_int8(x, q, a)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    ws = torch.zeros(woq.woq_workspace_bytes(4, M, N, K), dtype=torch.uint8, device=dev)
+
+    def launch(p):
+        if args.int8:
+            woq.woq_w4a8_gemv(p, q, a, N, K, y, ws)
+        else:
+            woq.woq_w4a8_linear_bf16(p, x, N, K, y, ws)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        launch(bufs[0])
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for p in bufs:
+            launch(p)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (args.steps * copies)
+    nbytes = N * K // 2 + 2 * N * (K // 128) + (M * K if args.int8 else 2 * M * K)
+    peak, kind = measured_peak()
+    print(json.dumps({"linear": args.linear, "K": K, "N": N, "m": M, "entry": "int8" if args.int8 else "bf16",
+                      "us_per_launch": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
+                      "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "peak_kind": kind,
+                      "launches_per_graph": copies}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.linear:
+        run_linear(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

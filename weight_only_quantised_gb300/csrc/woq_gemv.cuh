@@ -80,9 +80,19 @@ static __device__ unsigned long long g_trace[kTraceSlots * kTraceCtas * kTraceEv
       g_trace[((p.launch_id % kTraceSlots) * kTraceCtas + blockIdx.x) * kTraceEvents + (ev)] =        \
           dev::global_timer_ns();                                                                     \
   } while (0)
+#define WOQ_TRACE_EV2(ev)                                                                             \
+  do {                                                                                                \
+    if (blockIdx.x < kTraceCtas)                                                                      \
+      g_trace[((launch_id % kTraceSlots) * kTraceCtas + blockIdx.x) * kTraceEvents + (ev)] =          \
+          dev::global_timer_ns();                                                                     \
+  } while (0)
 #else
 #define WOQ_TRACE_EV(ev) \
   do {                   \
+  } while (0)
+#define WOQ_TRACE_EV2(ev) \
+  do {                    \
+    (void)launch_id;      \
   } while (0)
 #endif
 
@@ -270,35 +280,61 @@ struct StageCursor {
 
 // Activation prologue of the fused entry, run by the consumer warps on the bf16 x
 // that one bulk copy placed at act[0, 2 M K): per-row amax, scale = amax / 127, and
-// q = rne(x / scale) written in place over the first M K bytes.  Rounds of
-// kConsumers * 32 values, read fully before any thread writes, walk the rows in
-// order: q byte e overwrites only x bytes of values already read.
+// q = rne(x / scale) written in place over the first M K bytes (q byte e overwrites
+// only x bytes of values with index <= e).
+//
+// Small tiles (M K <= kConsumers * 8 * kRegVecs) are read once into registers; the
+// barrier after the amax pass then guarantees that every x value has been read
+// before any q byte is written.  Larger tiles are quantised in rounds, each read in
+// full before any thread of the round writes.
+constexpr int kRegVecs = 12;  // 8-value vectors per thread kept in registers
+
+// Eight bf16 values -> eight q bytes (two words), with the rare exact-division fallback.
+__device__ __forceinline__ uint2 quantise8(uint4 xv, float sc, float rc, bool valid) {
+  const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+  float xf[8];
+  uint32_t qb[8];
+  bool near = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    xf[i] = __uint_as_float((i & 1) ? (w4[i >> 1] & 0xFFFF0000u) : (w4[i >> 1] << 16));
+    bool nt;
+    qb[i] = dev::quant_byte_fast(__fmul_rn(xf[i], rc), nt);
+    near |= nt;
+  }
+  // rare: a lane of the warp holds a quotient within 3e-5 of a tie; divide there
+  if (__any_sync(0xffffffffu, near && valid)) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      bool nt;
+      dev::quant_byte_fast(__fmul_rn(xf[i], rc), nt);
+      if (nt) qb[i] = dev::quant_byte_exact(xf[i], sc);
+    }
+  }
+  if (sc == 0.0f) return make_uint2(0u, 0u);  // all-zero row
+  return make_uint2(qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24),
+                    qb[4] | (qb[5] << 8) | (qb[6] << 16) | (qb[7] << 24));
+}
+
+// max |x| over eight bf16 values (bf16 pairs, sign bits cleared; exact)
+__device__ __forceinline__ float absmax8(uint4 v) {
+  const uint32_t w4[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+  const __nv_bfloat162 a = __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w4[0]),
+                                           *reinterpret_cast<const __nv_bfloat162*>(&w4[1])),
+                                   __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w4[2]),
+                                           *reinterpret_cast<const __nv_bfloat162*>(&w4[3])));
+  return fmaxf(__low2float(a), __high2float(a));
+}
+
+// Per-row amax partials of this thread -> row scales and reciprocals (one barrier).
 template <int M>
-__device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, int lane, int warp, float* s_scratch,
-                                                  float* s_as) {
-  const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
-  // amax: bf16 pairs, |.| by clearing sign bits, max of bf16 values is exact
-  float lmax[M];
+__device__ __forceinline__ void row_scales(const float (&lmax)[M], int tid, int lane, int warp, float* s_scratch,
+                                           float* s_as, float (&sc)[M], float (&rc)[M]) {
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    __nv_bfloat162 a4[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a4[i] = __nv_bfloat162(__float2bfloat16_rn(0.0f), __float2bfloat16_rn(0.0f));
-    for (int e = tid * 8; e < K; e += kConsumers * 8) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xs + (size_t)m * K + e);
-      const uint32_t w4[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a4[i] = __hmax2(a4[i], *reinterpret_cast<const __nv_bfloat162*>(&w4[i]));
-    }
-    const __nv_bfloat162 a2 = __hmax2(__hmax2(a4[0], a4[1]), __hmax2(a4[2], a4[3]));
-    float a = fmaxf(__low2float(a2), __high2float(a2));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    lmax[m] = a;
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int m = 0; m < M; ++m) s_scratch[warp * 4 + m] = lmax[m];
+    // non-negative floats order like their bit patterns
+    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(lmax[m]));
+    if (lane == 0) s_scratch[warp * 4 + m] = __uint_as_float(wm);
   }
   dev::named_barrier_sync(kBarConsumers, kConsumers);
 #pragma unroll
@@ -306,10 +342,71 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, 
     float amax = s_scratch[m];
 #pragma unroll
     for (int w = 1; w < kCW; ++w) amax = fmaxf(amax, s_scratch[w * 4 + m]);
-    const float sc = __fdiv_rn(amax, 127.0f);
-    const float rc = __frcp_rn(sc);
-    if (tid == 0) s_as[m] = sc;
-    // this row's values, in rounds
+    sc[m] = __fdiv_rn(amax, 127.0f);
+    rc[m] = __frcp_rn(sc[m]);
+    if (tid == 0) s_as[m] = sc[m];
+  }
+}
+
+template <int M>
+__device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, int lane, int warp, float* s_scratch,
+                                                  float* s_as, int launch_id) {
+  const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
+  const int total = M * K;  // values, a multiple of 8 (K % 128 == 0)
+  float sc[M], rc[M];
+  if (total <= kConsumers * 8 * kRegVecs) {
+    // flat 8-value vectors v = tid + kConsumers * j; a vector lies within one row
+    uint4 xv[kRegVecs];
+    float lmax[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) lmax[m] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kRegVecs; ++j) {
+      const int e = 8 * (tid + kConsumers * j);
+      xv[j] = e < total ? *reinterpret_cast<const uint4*>(xs + e) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kRegVecs; ++j) {
+      const int e = 8 * (tid + kConsumers * j);
+      const float a = absmax8(xv[j]);  // zeros beyond the tile
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+        if (e >= m * K && e < (m + 1) * K) lmax[m] = fmaxf(lmax[m], a);
+    }
+    row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
+    if (tid == 0) WOQ_TRACE_EV2(5);
+#pragma unroll
+    for (int j = 0; j < kRegVecs; ++j) {
+      const int e = 8 * (tid + kConsumers * j);
+      if (8 * (kConsumers * j) >= total) break;  // warp-uniform: no vector of this j in range
+      int m = 0;
+#pragma unroll
+      for (int mm = 1; mm < M; ++mm) m += (e >= mm * K) ? 1 : 0;
+      float s = sc[0], r = rc[0];
+#pragma unroll
+      for (int mm = 1; mm < M; ++mm)
+        if (m == mm) {
+          s = sc[mm];
+          r = rc[mm];
+        }
+      const uint2 qv = quantise8(xv[j], s, r, e < total);
+      if (e < total) *reinterpret_cast<uint2*>(act + e) = qv;
+    }
+    return;
+  }
+  // larger tiles: amax pass, then rounds over each row
+  float lmax[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    float a = 0.0f;
+    for (int k = 8 * tid; k < K; k += kConsumers * 8)
+      a = fmaxf(a, absmax8(*reinterpret_cast<const uint4*>(xs + (size_t)m * K + k)));
+    lmax[m] = a;
+  }
+  row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);
+  if (tid == 0) WOQ_TRACE_EV2(5);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
     for (int k0 = 0; k0 < K; k0 += kConsumers * 32) {
       uint4 xv[4];
 #pragma unroll
@@ -318,42 +415,11 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, 
         xv[v] = k < K ? *reinterpret_cast<const uint4*>(xs + (size_t)m * K + k) : make_uint4(0, 0, 0, 0);
       }
       dev::named_barrier_sync(kBarConsumers, kConsumers);
-      if (sc == 0.0f) {  // all-zero row: q = 0 (row-uniform branch)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int k = k0 + 8 * (tid + kConsumers * v);
-          if (k < K) *reinterpret_cast<uint2*>(act + (size_t)m * K + k) = make_uint2(0u, 0u);
-        }
-        continue;
-      }
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const int k = k0 + 8 * (tid + kConsumers * v);
-        const uint32_t w4[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
-        float xf[8];
-        uint32_t qb[8];
-        bool near = false;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          xf[i] = __uint_as_float((i & 1) ? (w4[i >> 1] & 0xFFFF0000u) : (w4[i >> 1] << 16));
-          bool nt;
-          qb[i] = dev::quant_byte_fast(__fmul_rn(xf[i], rc), nt);
-          near |= nt;
-        }
-        // rare: a lane of the warp holds a quotient within 3e-5 of a tie; divide there
-        if (__any_sync(0xffffffffu, near && k < K)) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            bool nt;
-            dev::quant_byte_fast(__fmul_rn(xf[i], rc), nt);
-            if (nt) qb[i] = dev::quant_byte_exact(xf[i], sc);
-          }
-        }
-        if (k < K) {
-          const uint32_t lo = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
-          const uint32_t hi = qb[4] | (qb[5] << 8) | (qb[6] << 16) | (qb[7] << 24);
-          *reinterpret_cast<uint2*>(act + (size_t)m * K + k) = make_uint2(lo, hi);
-        }
+        const uint2 qv = quantise8(xv[v], sc[m], rc[m], k < K);
+        if (k < K) *reinterpret_cast<uint2*>(act + (size_t)m * K + k) = qv;
       }
     }
   }
@@ -496,7 +562,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
     }
   }
   if constexpr (FUSED) {
-    quantise_prologue<M>(act, p.K, tid, lane, warp, s_scratch, s_as);
+    quantise_prologue<M>(act, p.K, tid, lane, warp, s_scratch, s_as, p.launch_id);
   } else {
     if (tid < M) s_as[tid] = ascale_in;
   }
@@ -590,34 +656,55 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
               dev::st_relaxed_u64(mine + m * kTileRows + row, (1ull << 32) | __float_as_uint(sum[m]));
           }
         } else if (write_ok) {
+          if (tid == 0) WOQ_TRACE_EV(12 + (item == 0 ? 0 : 2));
+          // issue the loads of up to kBatch partner parts at once (one round trip), then poll
+          // only the words that were not there yet; sum in CTA order
+          constexpr int kBatch = M == 1 ? 8 : (M == 2 ? 4 : 2);  // bounded by registers
           float tot[M];
 #pragma unroll
           for (int m = 0; m < M; ++m) tot[m] = 0.0f;
           bool ok = true;
-          for (uint32_t c2 = c_first; c2 <= c_last; ++c2) {
-            if (c2 == cta) {
+          for (uint32_t cb = c_first; cb <= c_last; cb += kBatch) {
+            unsigned long long w[kBatch][M];
+            unsigned long long* src[kBatch];
 #pragma unroll
-              for (int m = 0; m < M; ++m) tot[m] = __fadd_rn(tot[m], sum[m]);
-              continue;
-            }
-            const int part2 = (t == range_begin(c2, p.NB, C) / (uint32_t)G) ? 0 : 1;
-            unsigned long long* src = p.parts + ((size_t)(c2 * 2 + part2) * M) * kTileRows;
+            for (int b = 0; b < kBatch; ++b) {
+              const uint32_t c2 = cb + b;
+              src[b] = nullptr;
+              if (c2 <= c_last && c2 != cta) {
+                const int part2 = (t == range_begin(c2, p.NB, C) / (uint32_t)G) ? 0 : 1;
+                src[b] = p.parts + ((size_t)(c2 * 2 + part2) * M) * kTileRows + row;
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-              unsigned long long w = dev::ld_relaxed_u64(src + m * kTileRows + row);
-              if (!(w >> 32)) {
-                const uint64_t t0 = dev::global_timer_ns();
-                while (!(w >> 32)) {
-                  if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) break;
-                  __nanosleep(100);
-                  w = dev::ld_relaxed_u64(src + m * kTileRows + row);
-                }
+                for (int m = 0; m < M; ++m) w[b][m] = dev::ld_relaxed_u64(src[b] + m * kTileRows);
               }
-              if (!(w >> 32)) ok = false;
-              tot[m] = __fadd_rn(tot[m], __uint_as_float((uint32_t)w));
-              dev::st_relaxed_u64(src + m * kTileRows + row, 0ull);  // ready for the next launch
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+              const uint32_t c2 = cb + b;
+              if (c2 > c_last) break;
+              if (c2 == cta) {
+#pragma unroll
+                for (int m = 0; m < M; ++m) tot[m] = __fadd_rn(tot[m], sum[m]);
+                continue;
+              }
+#pragma unroll
+              for (int m = 0; m < M; ++m) {
+                unsigned long long v = w[b][m];
+                if (!(v >> 32)) {
+                  const uint64_t t0 = dev::global_timer_ns();
+                  while (!(v >> 32)) {
+                    if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) break;
+                    __nanosleep(64);
+                    v = dev::ld_relaxed_u64(src[b] + m * kTileRows);
+                  }
+                }
+                if (!(v >> 32)) ok = false;
+                tot[m] = __fadd_rn(tot[m], __uint_as_float((uint32_t)v));
+                dev::st_relaxed_u64(src[b] + m * kTileRows, 0ull);  // ready for the next launch
+              }
             }
           }
+          if (tid == 0) WOQ_TRACE_EV(13 + (item == 0 ? 0 : 2));
           if (!ok) {
             atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
           } else if (n < p.N) {
