@@ -184,6 +184,25 @@ WOQ_API int woq_w6a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, cons
                          void* ws, size_t ws_bytes, woq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Allocation-free variant of woq_w4a8_linear_bf16 (the pages have no counterpart:
+ * this is a service for callers that cannot allocate device memory, such as
+ * plugins inside a host application that owns every device allocation, or loops
+ * with a fixed memory budget where a cudaMalloc could synchronise or fail).
+ *   Same inputs and outputs as woq_w4a8_linear_bf16, without a workspace: its
+ *   scratch is a 2 MiB array built into the library, present on every GPU that
+ *   loads it until the process exits (enough for M <= 4 with grids of up to 255
+ *   CTAs; a shape whose launch would need more returns WOQ_ERR_WORKSPACE).
+ *   The first call on each device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.  Every call
+ *   zeroes the part of the scratch it uses (an asynchronous memset on the stream)
+ *   and then launches the linear; it allocates nothing.  All calls share the one
+ *   array, so calls that can overlap on the GPU (different streams, or a woq
+ *   linear/GEMV launch running at the same time) race and must be avoided.
+ * --------------------------------------------------------------------------- */
+WOQ_API int woq_w4a8_linear_bf16_noalloc(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N,
+                                         int K, float* y, woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Debug: the exact per-group integer dot products the GEMV scales.
  *   dots: device int32 [M][N][K/128]; dots[m][n][g] = sum over k in group g of
  *   w(n, k) * q(m, k).  Same bounds as the GEMV (no workspace).

@@ -59,6 +59,7 @@ _SIGS = {
     "woq_w4a8_linear_bf16": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
     "woq_w6a8_linear_bf16": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
     "woq_debug_group_dots": ([_I, _P, _Z, _P, _I, _I, _I, _P, _P], _I),
+    "woq_w4a8_linear_bf16_noalloc": ([_P, _Z, _P, _I, _I, _I, _P, _P], _I),
     "woq_tune_override": ([_I, _I, _I], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -204,6 +205,14 @@ def woq_w4a8_linear_bf16(wpacked, x_bf16, N: int, K: int, y, ws, stream=None) ->
 
 def woq_w6a8_linear_bf16(wpacked, x_bf16, N: int, K: int, y, ws, stream=None) -> None:
     _linear(lib.woq_w6a8_linear_bf16, "woq_w6a8_linear_bf16", wpacked, x_bf16, N, K, y, ws, stream)
+
+
+def woq_w4a8_linear_bf16_noalloc(wpacked, x_bf16, N: int, K: int, y, stream=None) -> None:
+    """woq_w4a8_linear_bf16 for callers that cannot allocate a workspace (the library's own
+    2 MiB scratch is used; calls that overlap on the GPU race)."""
+    M = x_bf16.shape[0]
+    _check(lib.woq_w4a8_linear_bf16_noalloc(_dptr(wpacked), _nbytes(wpacked), _dptr(x_bf16), M, N, K, _dptr(y),
+                                            _stream(stream)), "woq_w4a8_linear_bf16_noalloc")
 
 
 def woq_debug_group_dots(bits: int, wpacked, q, N: int, K: int, dots, stream=None) -> None:

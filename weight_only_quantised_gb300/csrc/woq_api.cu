@@ -292,11 +292,68 @@ int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_bytes, co
                                                                                                   : WOQ_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the int4 bf16 linear.
+//
+// Some callers cannot allocate device memory for a workspace: plugins that run inside
+// a host application which owns every device allocation, and latency-critical loops
+// with a fixed memory budget, where a cudaMalloc could synchronise the device or fail
+// at run time.  This entry point needs no workspace from them: its scratch is a
+// file-scope device array below, part of this library's image on every GPU that
+// loads it and kept until the process exits.
+static constexpr size_t kNoAllocScratchBytes = 2u << 20;  // 2 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+}  // namespace
+
+// Device address of the scratch array on the current device.  The array's name is only a
+// host-side stand-in in host code, so the address is looked up once per device (with that
+// device current) and cached.
+static int noalloc_scratch(void** out) {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return WOQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[d] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return WOQ_ERR_CUDA;
+    g_noalloc_ptr[d] = ptr;
+  }
+  *out = g_noalloc_ptr[d];
+  return WOQ_OK;
+}
+
 #ifdef WOQ_TRACE
 // Trace build only: the id the next GEMV / linear launch will get.
 __attribute__((visibility("default"))) int woq_trace_next_launch_id(void) {
   return g_launch_counter.load() & 0x7fffffff;
 }
 #endif
+
+int woq_w4a8_linear_bf16_noalloc(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K,
+                                 float* y, woq_stream_t stream) {
+  if (M < 0 || M > kMaxM || N < 0 || K < 0 || K % kGroup || (long)M * K > kMaxMK) return WOQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return WOQ_OK;
+  if (!y || (K > 0 && (!wpacked || !x_bf16))) return WOQ_ERR_NULL;
+  if (!aligned(y, 4) || (K > 0 && (!aligned(wpacked, 16) || !aligned(x_bf16, 16)))) return WOQ_ERR_ALIGN;
+  if (K > 0 && wpacked_bytes < packed_bytes(4, N, K)) return WOQ_ERR_LAYOUT;
+  // the scratch this launch will use must fit in the static array
+  size_t need = 256;
+  if (K > 0) {
+    const LaunchConfig cfg = choose_config(4, M, N, K, true);
+    if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
+    need = workspace_layout(M, N, cfg.ctas).total;
+  }
+  if (need > kNoAllocScratchBytes) return WOQ_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const int st = noalloc_scratch(&ws);
+  if (st != WOQ_OK) return st;
+  // the array keeps the previous call's contents: start from zero (no allocation involved)
+  if (cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream) != cudaSuccess) return WOQ_ERR_CUDA;
+  return run_gemv(4, true, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, M, N, K, y, ws, kNoAllocScratchBytes,
+                  (cudaStream_t)stream);
+}
 
 }  // extern "C"
