@@ -97,8 +97,11 @@ LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
   }
   if (stages < 2) return cfg;
   const int stage_bytes = kStageBlocks * block_bytes(bits);
+  // L2 prefetch window beyond the ring: one stage by default.  A deeper window puts the
+  // next launch's whole share in the memory queues at once, and the small critical-path
+  // reads of the running launch (activations, split-tile partials) then wait behind it.
   int pf_kb = g_override_prefetch_kb.load(std::memory_order_relaxed);
-  if (pf_kb < 0) pf_kb = 256;
+  if (pf_kb < 0) pf_kb = stage_bytes / 1024;
   // at least one stage (kStageBlocks blocks) of work per CTA
   long long ctas = (long long)sms * cps;
   const long long by_work = (NB + kStageBlocks - 1) / kStageBlocks;

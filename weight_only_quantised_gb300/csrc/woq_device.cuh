@@ -143,6 +143,47 @@ __device__ __forceinline__ uint32_t quant_byte_exact(float x, float s) {
   return (uint32_t)(int)rintf(__fdiv_rn(x, s)) & 0xFFu;
 }
 
+// Pairs of fp32 in one 64-bit register (low word = first element), with the packed
+// round-to-nearest pair arithmetic of the sm_100 family.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_pack(uint32_t lo, uint32_t hi) { return ((f32x2)hi << 32) | lo; }
+__device__ __forceinline__ f32x2 f2_splat(float v) { return f2_pack(__float_as_uint(v), __float_as_uint(v)); }
+__device__ __forceinline__ uint32_t f2_lo(f32x2 v) { return (uint32_t)v; }
+__device__ __forceinline__ uint32_t f2_hi(f32x2 v) { return (uint32_t)(v >> 32); }
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Per half: the value of larger magnitude, with sign bit = xor of the two signs.  Chained,
+// the magnitude in each half is the running max |x| (exact; bf16 pairs).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// max |x| of a bf16x2 absmax accumulator, as an fp32 (exact)
+__device__ __forceinline__ float bf16x2_absmax_to_float(uint32_t acc) {
+  return fmaxf(__uint_as_float((acc & 0x7FFFu) << 16), __uint_as_float(acc & 0x7FFF0000u));
+}
+
 // 64-bit relaxed global load / store at GPU scope (single-copy atomic for aligned words).
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;

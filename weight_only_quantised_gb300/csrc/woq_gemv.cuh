@@ -15,24 +15,27 @@
 //   * One CTA per SM (persistent).  The matrix's blocks (128 rows x 128 k) are
 //     dealt out as equal contiguous ranges, one per CTA, so every SM streams
 //     the same number of bytes whatever N and K are.  A 128-row tile cut by a
-//     range boundary is finished by the last of its CTAs to arrive (partial sums
-//     in the workspace plus a ticket counter; no spin-waits, fixed summation
-//     order, so results are deterministic).  Each CTA works on its two cut tiles
-//     first, so the fix-up is off the launch's critical tail.
-//   * Warp 4 is the producer: one lane issues 1-D bulk copies (TMA engine) of
+//     range boundary is finished by one statically chosen CTA of those sharing
+//     it (the one whose part is expected to end last): the others publish their
+//     partial sums as tagged 64-bit words in the workspace, the combiner polls
+//     for them (bounded), sums them in CTA order and clears them, so results are
+//     deterministic.  Each CTA works on its two cut tiles first, so the fix-up
+//     is off the launch's critical tail.
+//   * Warp 8 is the producer: one lane issues 1-D bulk copies (TMA engine) of
 //     whole stages (4 consecutive blocks of one tile, 33 KB for int4) into a
 //     small ring of shared-memory stages tracked by mbarriers (L2 evict-first:
-//     every weight byte is read once), and keeps a window of later stages in
-//     flight from HBM into L2 with bulk L2 prefetches, so the bytes in flight do
-//     not depend on the ring's size.  The small ring lets the CTA of the next
-//     launch share the SM and start its weight stream before this one ends.
-//   * Warps 0..3 consume: warp w takes block w of each stage.  Lane l owns rows
-//     l, 32+l, 64+l, 96+l of the tile; for each 32-k quarter it reads its
-//     16-byte chunk per row (consecutive lanes, conflict-free) and the quarter's
-//     activations (same address for all lanes: a broadcast), unpacks int4 (or
-//     int6) to int8 lanes with two masks and a shift, and runs dp4a.  Per group
-//     the int32 dot is exact; the term (d * wscale) * ascale is formed with two
-//     fp32 roundings, as in the definition, and accumulated in fp32.
+//     every weight byte is read once), and keeps a short window of later stages
+//     in flight from HBM into L2 with bulk L2 prefetches.  The small ring lets
+//     the CTA of the next launch share the SM and start its weight stream
+//     before this one ends.
+//   * Warps 0..7 consume: warp w takes rows 64(w&1) .. 64(w&1)+63 of block w>>1
+//     of each stage.  Lane l owns two rows of that half; for each 32-k quarter
+//     it reads its 16-byte chunk per row (consecutive lanes, conflict-free) and
+//     the quarter's activations (same address for all lanes: a broadcast),
+//     unpacks int4 (or int6) to int8 lanes with masks and shifts, and runs
+//     dp4a.  Per group the int32 dot is exact; the term (d * wscale) * ascale is
+//     formed with two fp32 roundings, as in the definition, and accumulated in
+//     fp32.
 //   * The activations arrive with one bulk copy and stay in shared memory for the
 //     whole launch.  The fused entry copies bf16 x, takes the per-row amax and
 //     quantises it in place, bit-identical to the standalone kernel.
@@ -47,6 +50,7 @@
 
 #include "woq_device.cuh"
 #include "woq_layout.h"
+#include "woq_scale_table.h"
 
 namespace woq {
 
@@ -72,7 +76,7 @@ struct GemvParams {
 // Trace build only: %globaltimer stamps per (launch slot, CTA, event); no atomics.
 constexpr int kTraceSlots = 16;
 constexpr int kTraceCtas = 512;
-constexpr int kTraceEvents = 16;
+constexpr int kTraceEvents = 64;  // 0..15 phases, 16+s stage s ready (warp 0), 32+i ring load i issued, 48.. combine
 static __device__ unsigned long long g_trace[kTraceSlots * kTraceCtas * kTraceEvents];
 #define WOQ_TRACE_EV(ev)                                                                              \
   do {                                                                                                \
@@ -283,50 +287,78 @@ struct StageCursor {
 // q = rne(x / scale) written in place over the first M K bytes (q byte e overwrites
 // only x bytes of values with index <= e).
 //
-// Small tiles (M K <= kConsumers * 8 * kRegVecs) are read once into registers; the
+// Rows with K <= kConsumers * 8 * (kRegVecs / M) are read once into registers; the
 // barrier after the amax pass then guarantees that every x value has been read
-// before any q byte is written.  Larger tiles are quantised in rounds, each read in
-// full before any thread of the round writes.
+// before any q byte is written.  Longer rows are quantised in rounds, each read in
+// full before any thread of the round writes.  Every vector is stored as the fast
+// route gives it; one warp vote afterwards sends the rare vectors with a quotient
+// near a tie through the exact route, which stores them again.
 constexpr int kRegVecs = 12;  // 8-value vectors per thread kept in registers
 
-// Eight bf16 values -> eight q bytes (two words), with the rare exact-division fallback.
-__device__ __forceinline__ uint2 quantise8(uint4 xv, float sc, float rc, bool valid) {
+// Row scale s = RN(amax / 127) and rc = RN(1 / s) for a bf16 amax held in an fp32.
+// For 2^-119 <= amax < inf, amax = A 2^e with A = 1 + f/128 and the significand
+// tables hold RN(A / 127) and RN(1 / RN(A / 127)); a power of two passes through
+// round-to-nearest unchanged while the result stays normal, so both are exact.
+// Zero, tiny and non-finite amax take the IEEE division and reciprocal.
+__device__ __forceinline__ void scale_and_rcp(float amax, float& s, float& rc) {
+  const uint32_t b = __float_as_uint(amax);
+  const uint32_t e = b >> 23;  // biased exponent (amax >= 0)
+  if (e >= 8u && e < 255u) {
+    const uint32_t f = (b >> 16) & 0x7Fu;
+    const uint32_t sh = (e - 127u) << 23;  // two's complement exponent shift
+    s = __uint_as_float(kScaleSig[f] + sh);
+    rc = __uint_as_float(kRcpSig[f] - sh);
+  } else {
+    s = __fdiv_rn(amax, 127.0f);
+    rc = __frcp_rn(s);
+  }
+}
+
+// Eight bf16 values -> eight q bytes by the fast route, the pairs in packed fp32x2
+// arithmetic: t = RN(x rc); y = RN(t + 1.5 2^23), whose low byte is rne(t) mod 256;
+// d = t - rne(t) (exact); g = RN(d d - kTieGuard^2).  `gand` keeps the AND of the g
+// words: its sign bit stays set only while every |d| is below kTieGuard (with a margin
+// far above the rounding of g), i.e. while no value of the vector needs the exact route.
+__device__ __forceinline__ uint2 quantise8_fast(uint4 xv, dev::f32x2 rc2, uint32_t& gand) {
+  constexpr float kGuardSq = dev::kTieGuard * dev::kTieGuard;
+  const dev::f32x2 magic = dev::f2_splat(dev::kRoundMagic);
+  const dev::f32x2 nguard = dev::f2_splat(-kGuardSq);
   const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
-  float xf[8];
+  uint32_t yb[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const dev::f32x2 x = dev::f2_pack(w4[i] << 16, w4[i] & 0xFFFF0000u);  // values 2i, 2i+1
+    const dev::f32x2 t = dev::f2_mul(x, rc2);
+    const dev::f32x2 y = dev::f2_add(t, magic);
+    const dev::f32x2 d = dev::f2_sub(t, dev::f2_sub(y, magic));
+    const dev::f32x2 g = dev::f2_fma(d, d, nguard);
+    gand &= dev::f2_lo(g) & dev::f2_hi(g);
+    yb[2 * i] = dev::f2_lo(y);
+    yb[2 * i + 1] = dev::f2_hi(y);
+  }
+  return make_uint2(__byte_perm(__byte_perm(yb[0], yb[1], 0x0040), __byte_perm(yb[2], yb[3], 0x0040), 0x5410),
+                    __byte_perm(__byte_perm(yb[4], yb[5], 0x0040), __byte_perm(yb[6], yb[7], 0x0040), 0x5410));
+}
+
+// Eight q bytes by the IEEE division; kept out of line so the common path carries no
+// division code.
+static __device__ __noinline__ uint2 quantise8_exact(uint4 xv, float sc) {
+  const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
   uint32_t qb[8];
-  bool near = false;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    xf[i] = __uint_as_float((i & 1) ? (w4[i >> 1] & 0xFFFF0000u) : (w4[i >> 1] << 16));
-    bool nt;
-    qb[i] = dev::quant_byte_fast(__fmul_rn(xf[i], rc), nt);
-    near |= nt;
-  }
-  // rare: a lane of the warp holds a quotient within 3e-5 of a tie; divide there
-  if (__any_sync(0xffffffffu, near && valid)) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      bool nt;
-      dev::quant_byte_fast(__fmul_rn(xf[i], rc), nt);
-      if (nt) qb[i] = dev::quant_byte_exact(xf[i], sc);
-    }
-  }
-  if (sc == 0.0f) return make_uint2(0u, 0u);  // all-zero row
+  for (int i = 0; i < 8; ++i)
+    qb[i] = dev::quant_byte_exact(__uint_as_float((i & 1) ? (w4[i >> 1] & 0xFFFF0000u) : (w4[i >> 1] << 16)), sc);
   return make_uint2(qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24),
                     qb[4] | (qb[5] << 8) | (qb[6] << 16) | (qb[7] << 24));
 }
 
-// max |x| over eight bf16 values (bf16 pairs, sign bits cleared; exact)
-__device__ __forceinline__ float absmax8(uint4 v) {
-  const uint32_t w4[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
-  const __nv_bfloat162 a = __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w4[0]),
-                                           *reinterpret_cast<const __nv_bfloat162*>(&w4[1])),
-                                   __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w4[2]),
-                                           *reinterpret_cast<const __nv_bfloat162*>(&w4[3])));
-  return fmaxf(__low2float(a), __high2float(a));
+// bf16x2 absmax accumulator over one 8-value vector
+__device__ __forceinline__ uint32_t absmax8(uint32_t acc, uint4 v) {
+  return dev::bf16x2_absmax(acc, dev::bf16x2_absmax(dev::bf16x2_absmax(v.x, v.y), dev::bf16x2_absmax(v.z, v.w)));
 }
 
-// Per-row amax partials of this thread -> row scales and reciprocals (one barrier).
+// Per-row amax partials of this thread -> every thread's row scales and reciprocals
+// (one barrier).  s_scratch holds [4 rows][8 warps] partials.
 template <int M>
 __device__ __forceinline__ void row_scales(const float (&lmax)[M], int tid, int lane, int warp, float* s_scratch,
                                            float* s_as, float (&sc)[M], float (&rc)[M]) {
@@ -334,92 +366,125 @@ __device__ __forceinline__ void row_scales(const float (&lmax)[M], int tid, int 
   for (int m = 0; m < M; ++m) {
     // non-negative floats order like their bit patterns
     const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(lmax[m]));
-    if (lane == 0) s_scratch[warp * 4 + m] = __uint_as_float(wm);
+    if (lane == 0) s_scratch[m * kCW + warp] = __uint_as_float(wm);
   }
   dev::named_barrier_sync(kBarConsumers, kConsumers);
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    float amax = s_scratch[m];
-#pragma unroll
-    for (int w = 1; w < kCW; ++w) amax = fmaxf(amax, s_scratch[w * 4 + m]);
-    sc[m] = __fdiv_rn(amax, 127.0f);
-    rc[m] = __frcp_rn(sc[m]);
+    const float4 a = *reinterpret_cast<const float4*>(s_scratch + m * kCW);
+    const float4 b = *reinterpret_cast<const float4*>(s_scratch + m * kCW + 4);
+    const float amax = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+    scale_and_rcp(amax, sc[m], rc[m]);
     if (tid == 0) s_as[m] = sc[m];
   }
+}
+
+// Fast-route gate of a row: all ones when the fast route may decide (rc finite, or an
+// all-zero row, stored as zeros), else zero so that every vector of the row is redone.
+__device__ __forceinline__ uint32_t row_gate(float sc, float rc) {
+  return (sc == 0.0f || rc <= 3.4028234e38f) ? 0xFFFFFFFFu : 0u;
 }
 
 template <int M>
 __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, int lane, int warp, float* s_scratch,
                                                   float* s_as, int launch_id) {
+  constexpr int kVPR = kRegVecs / M;  // vectors per row held in registers
+  constexpr int kStride = kConsumers * 8;  // values per vector round of all threads
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
-  const int total = M * K;  // values, a multiple of 8 (K % 128 == 0)
   float sc[M], rc[M];
-  if (total <= kConsumers * 8 * kRegVecs) {
-    // flat 8-value vectors v = tid + kConsumers * j; a vector lies within one row
-    uint4 xv[kRegVecs];
+  if (K <= kStride * kVPR) {
+    uint4 xv[M][kVPR];
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+      for (int j = 0; j < kVPR; ++j) {
+        const int k = 8 * tid + kStride * j;
+        xv[m][j] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
+      }
     float lmax[M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) lmax[m] = 0.0f;
+    for (int m = 0; m < M; ++m) {
+      uint32_t acc = 0;
 #pragma unroll
-    for (int j = 0; j < kRegVecs; ++j) {
-      const int e = 8 * (tid + kConsumers * j);
-      xv[j] = e < total ? *reinterpret_cast<const uint4*>(xs + e) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int j = 0; j < kRegVecs; ++j) {
-      const int e = 8 * (tid + kConsumers * j);
-      const float a = absmax8(xv[j]);  // zeros beyond the tile
-#pragma unroll
-      for (int m = 0; m < M; ++m)
-        if (e >= m * K && e < (m + 1) * K) lmax[m] = fmaxf(lmax[m], a);
+      for (int j = 0; j < kVPR; ++j) {
+        if (kStride * j >= K) break;  // warp-uniform
+        acc = absmax8(acc, xv[m][j]);  // zeros beyond the row
+      }
+      lmax[m] = dev::bf16x2_absmax_to_float(acc);
     }
     row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
     if (tid == 0) WOQ_TRACE_EV2(5);
+    uint32_t redo = 0;  // bit m * kVPR + j
 #pragma unroll
-    for (int j = 0; j < kRegVecs; ++j) {
-      const int e = 8 * (tid + kConsumers * j);
-      if (8 * (kConsumers * j) >= total) break;  // warp-uniform: no vector of this j in range
-      int m = 0;
+    for (int m = 0; m < M; ++m) {
+      const dev::f32x2 rc2 = dev::f2_splat(rc[m]);
+      const uint32_t gate = row_gate(sc[m], rc[m]);
 #pragma unroll
-      for (int mm = 1; mm < M; ++mm) m += (e >= mm * K) ? 1 : 0;
-      float s = sc[0], r = rc[0];
-#pragma unroll
-      for (int mm = 1; mm < M; ++mm)
-        if (m == mm) {
-          s = sc[mm];
-          r = rc[mm];
+      for (int j = 0; j < kVPR; ++j) {
+        if (kStride * j >= K) break;
+        const int k = 8 * tid + kStride * j;
+        uint32_t g = gate;
+        const uint2 q = quantise8_fast(xv[m][j], rc2, g);
+        if (k < K) {
+          *reinterpret_cast<uint2*>(act + m * K + k) = sc[m] == 0.0f ? make_uint2(0u, 0u) : q;
+          if (!(g >> 31) && sc[m] != 0.0f) redo |= 1u << (m * kVPR + j);
         }
-      const uint2 qv = quantise8(xv[j], s, r, e < total);
-      if (e < total) *reinterpret_cast<uint2*>(act + e) = qv;
+      }
+    }
+    if (__any_sync(0xffffffffu, redo != 0)) {  // rare
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int j = 0; j < kVPR; ++j)
+          if (redo & (1u << (m * kVPR + j)))
+            *reinterpret_cast<uint2*>(act + m * K + 8 * tid + kStride * j) = quantise8_exact(xv[m][j], sc[m]);
     }
     return;
   }
-  // larger tiles: amax pass, then rounds over each row
+  // longer rows: amax pass, then rounds of 4 vectors per thread over each row
   float lmax[M];
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    float a = 0.0f;
-    for (int k = 8 * tid; k < K; k += kConsumers * 8)
-      a = fmaxf(a, absmax8(*reinterpret_cast<const uint4*>(xs + (size_t)m * K + k)));
-    lmax[m] = a;
+    uint32_t a[4] = {0u, 0u, 0u, 0u};
+    int k = 8 * tid;
+    for (; k + 3 * kStride < K; k += 4 * kStride) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = absmax8(a[u], *reinterpret_cast<const uint4*>(xs + m * K + k + u * kStride));
+    }
+    for (; k < K; k += kStride) a[0] = absmax8(a[0], *reinterpret_cast<const uint4*>(xs + m * K + k));
+    lmax[m] = dev::bf16x2_absmax_to_float(dev::bf16x2_absmax(dev::bf16x2_absmax(a[0], a[1]),
+                                                             dev::bf16x2_absmax(a[2], a[3])));
   }
   row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);
   if (tid == 0) WOQ_TRACE_EV2(5);
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    for (int k0 = 0; k0 < K; k0 += kConsumers * 32) {
+    const dev::f32x2 rc2 = dev::f2_splat(rc[m]);
+    const uint32_t gate = row_gate(sc[m], rc[m]);
+    for (int k0 = 0; k0 < K; k0 += 4 * kStride) {
       uint4 xv[4];
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const int k = k0 + 8 * (tid + kConsumers * v);
-        xv[v] = k < K ? *reinterpret_cast<const uint4*>(xs + (size_t)m * K + k) : make_uint4(0, 0, 0, 0);
+        const int k = k0 + 8 * tid + kStride * v;
+        xv[v] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
       }
       dev::named_barrier_sync(kBarConsumers, kConsumers);
+      uint32_t redo = 0;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const int k = k0 + 8 * (tid + kConsumers * v);
-        const uint2 qv = quantise8(xv[v], sc[m], rc[m], k < K);
-        if (k < K) *reinterpret_cast<uint2*>(act + (size_t)m * K + k) = qv;
+        const int k = k0 + 8 * tid + kStride * v;
+        uint32_t g = gate;
+        const uint2 q = quantise8_fast(xv[v], rc2, g);
+        if (k < K) {
+          *reinterpret_cast<uint2*>(act + m * K + k) = sc[m] == 0.0f ? make_uint2(0u, 0u) : q;
+          if (!(g >> 31) && sc[m] != 0.0f) redo |= 1u << v;
+        }
+      }
+      if (__any_sync(0xffffffffu, redo != 0)) {  // rare
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          if (redo & (1u << v))
+            *reinterpret_cast<uint2*>(act + m * K + k0 + 8 * tid + kStride * v) = quantise8_exact(xv[v], sc[m]);
       }
     }
   }
@@ -435,7 +500,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
   uint64_t* actbar = full + 16;                                // activations landed
   volatile int* s_flags = reinterpret_cast<volatile int*>(smem + 136);  // [0] ticket-last, [1] abort, [2] header-ok
   float* s_as = reinterpret_cast<float*>(smem + 160);          // [M] activation scales
-  float* s_scratch = reinterpret_cast<float*>(smem + 192);     // [8 warps][4 rows] amax partials, to byte 320
+  float* s_scratch = reinterpret_cast<float*>(smem + 192);     // [4 rows][8 warps] amax partials, to byte 320
   uint8_t* act = smem + p.act_offset;                          // bf16 x, quantised in place (fused) or int8 q
   float* red = reinterpret_cast<float*>(smem + p.red_offset);  // [4 blocks][M][128 rows]
   uint8_t* ring = smem + p.ring_offset;
@@ -482,6 +547,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
         const uint32_t bytes = (uint32_t)(ld.nb() * BB);
         dev::mbar_arrive_expect_tx(full + slot, bytes);
         dev::bulk_copy_g2s(ring + (size_t)slot * kStageBytes, blocks + (size_t)ld.block() * BB, bytes, full + slot, pol);
+        if (it < 16) WOQ_TRACE_EV(32 + (int)it);
       }
       WOQ_TRACE_EV(1);
       // keep prefetch_stages stages beyond the ring in flight into L2
@@ -498,6 +564,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
         const uint32_t bytes = (uint32_t)(ld.nb() * BB);
         dev::mbar_arrive_expect_tx(full + slot, bytes);
         dev::bulk_copy_g2s(ring + (size_t)slot * kStageBytes, blocks + (size_t)ld.block() * BB, bytes, full + slot, pol);
+        if (it < 16) WOQ_TRACE_EV(32 + (int)it);
         if (pf.valid()) {
           dev::bulk_prefetch_l2(blocks + (size_t)pf.block() * BB, (uint32_t)(pf.nb() * BB));
           pf.advance();
@@ -513,6 +580,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
       dev::mbar_wait_bounded(actbar, 0);
       const long long first = it > stages ? it - stages : 0;
       for (long long i = first; i < it; ++i) dev::mbar_wait_bounded(full + (int)(i % stages), (uint32_t)((i / stages) & 1));
+      WOQ_TRACE_EV(2);
     }
     return;
   }
@@ -520,15 +588,30 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
   // -------------------------------------------------------------------- consumers
   // roles in the split tiles (only the first two items can be split), worked out while the
   // previous grid may still be running
+  // (per split item: whether this CTA combines it, the first and last CTA sharing the tile,
+  // and which part slot the first of them publishes it in; a later sharer starts its range
+  // inside the tile, so the tile is its first part)
   bool comb0 = false, comb1 = false;
+  uint32_t cf0 = 0, cl0 = 0, cf1 = 0, cl1 = 0;
+  int fp0 = 0, fp1 = 0;
   {
     uint32_t t;
     int ga, gb;
     order.get(0, t, ga, gb);
-    if (!(ga == 0 && gb == G)) comb0 = is_combiner(cta, t, p.NB, C, (uint32_t)G);
+    if (!(ga == 0 && gb == G)) {
+      comb0 = is_combiner(cta, t, p.NB, C, (uint32_t)G);
+      cf0 = cta_of_block(t * G, p.NB, C);
+      cl0 = cta_of_block(t * G + G - 1, p.NB, C);
+      fp0 = range_begin(cf0, p.NB, C) < t * (uint32_t)G ? 1 : 0;
+    }
     if (order.n_items > 1) {
       order.get(1, t, ga, gb);
-      if (!(ga == 0 && gb == G)) comb1 = is_combiner(cta, t, p.NB, C, (uint32_t)G);
+      if (!(ga == 0 && gb == G)) {
+        comb1 = is_combiner(cta, t, p.NB, C, (uint32_t)G);
+        cf1 = cta_of_block(t * G, p.NB, C);
+        cl1 = cta_of_block(t * G + G - 1, p.NB, C);
+        fp1 = range_begin(cf1, p.NB, C) < t * (uint32_t)G ? 1 : 0;
+      }
     }
   }
   // activations (and y, the workspace) belong to the previous grid until it has completed
@@ -580,6 +663,9 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
   int slot = 0;
   uint32_t phase = 0;  // parity of the full-barrier phase to wait for
   bool first_stage = true;
+#ifdef WOQ_TRACE
+  int n_stage = 0;
+#endif
   for (int item = 0; item < order.n_items; ++item) {
     uint32_t t;
     int ga, gb;
@@ -600,6 +686,10 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
       }
       if (tid == 0 && first_stage) WOQ_TRACE_EV(7);
       first_stage = false;
+#ifdef WOQ_TRACE
+      if (tid == 0 && n_stage < 16) WOQ_TRACE_EV(16 + n_stage);
+      ++n_stage;
+#endif
       if (!aborted && hb < nb)
         consume_half_block<BITS, M>(ring + (size_t)slot * kStageBytes + (size_t)hb * BB, actq, p.K, g0 + hb, lane, hh,
                                     as, acc);
@@ -644,8 +734,9 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
       // the tag sees the value) and moves on.  No atomics, no barrier: the combiner polls
       // (bounded) and clears the words for the next launch.
       if (row_thread) {
-        const uint32_t c_first = cta_of_block(t * G, p.NB, C);
-        const uint32_t c_last = cta_of_block(t * G + G - 1, p.NB, C);
+        const uint32_t c_first = item == 0 ? cf0 : cf1;
+        const uint32_t c_last = item == 0 ? cl0 : cl1;
+        const int first_part = item == 0 ? fp0 : fp1;
         const bool comb = item == 0 ? comb0 : comb1;
         if (!comb) {
           if (write_ok) {
@@ -672,12 +763,13 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
               const uint32_t c2 = cb + b;
               src[b] = nullptr;
               if (c2 <= c_last && c2 != cta) {
-                const int part2 = (t == range_begin(c2, p.NB, C) / (uint32_t)G) ? 0 : 1;
+                const int part2 = c2 == c_first ? first_part : 0;
                 src[b] = p.parts + ((size_t)(c2 * 2 + part2) * M) * kTileRows + row;
 #pragma unroll
                 for (int m = 0; m < M; ++m) w[b][m] = dev::ld_relaxed_u64(src[b] + m * kTileRows);
               }
             }
+            if (tid == 0 && cb == c_first) WOQ_TRACE_EV(48 + (item == 0 ? 0 : 2));
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
               const uint32_t c2 = cb + b;
@@ -699,6 +791,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
                   }
                 }
                 if (!(v >> 32)) ok = false;
+                if (tid == 0 && cb == c_first) WOQ_TRACE_EV(49 + (item == 0 ? 0 : 2));
                 tot[m] = __fadd_rn(tot[m], __uint_as_float((uint32_t)v));
                 dev::st_relaxed_u64(src[b] + m * kTileRows, 0ull);  // ready for the next launch
               }
