@@ -220,6 +220,13 @@ WOQ_API int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_b
  * --------------------------------------------------------------------------- */
 WOQ_API int woq_tune_override(int ctas_per_sm, int stages, int prefetch_kb);
 
+/* Tuning: which consumer the following int4 GEMV / linear launches of this process
+ * use: 0 = launch table (dp4a), 1 = dp4a, 2 = f16 tensor-core MMA.  Both form the
+ * same exact per-group integer dots; outputs agree within the GEMV tolerance.
+ * int6 launches always use dp4a.  Not thread-safe; meant for benchmarks and
+ * tests.  WOQ_ERR_SHAPE for other values. */
+WOQ_API int woq_tune_path(int path);
+
 #ifdef __cplusplus
 }
 #endif

@@ -3,7 +3,8 @@
 Bars: act_quant (q bytes and scale bits) and the per-group dot products are
 bit-exact; y is within |y_gpu - y_ref| <= 1e-5 * sum_g |term_g| + 1e-6 per
 element; the fused bf16 entry is bit-identical to act_quant followed by the
-GEMV; repeated launches are bit-identical.  Inputs are the seeded synthetic
+GEMV; repeated launches are bit-identical.  The int4 GEMV / linear tests run
+with each consumer forced (dp4a, and the tensor-core MMA); int6 always uses dp4a.  Inputs are the seeded synthetic
 workloads (synthetic.py).  Guard regions around outputs and workspace catch
 writes out of bounds.
 """
@@ -29,6 +30,20 @@ def _gpu():
     torch.cuda.set_device(0)
     yield
     woq.woq_tune_override(0, 0, -1)
+    woq.woq_tune_path(0)
+
+
+DP4A, MMA = 1, 2
+BITS_PATHS = [(4, DP4A), (4, MMA), (6, DP4A)]
+
+
+@pytest.fixture()
+def consumer():
+    """Force the int4 consumer for one test: consumer(path)."""
+    def set_path(path):
+        woq.woq_tune_path(path)
+    yield set_path
+    woq.woq_tune_path(0)
 
 
 DEV = "cuda:0"
@@ -151,10 +166,11 @@ def test_group_dots_bit_exact(bits, M, N, K):
 SHAPES = [(1024, 1024), (1000, 1024), (300, 384), (129, 128), (4096, 512), (640, 2048)]
 
 
-@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("bits,path", BITS_PATHS)
 @pytest.mark.parametrize("M", [1, 2, 3, 4])
 @pytest.mark.parametrize("N,K", SHAPES)
-def test_gemv_matches_oracle(bits, M, N, K):
+def test_gemv_matches_oracle(bits, path, M, N, K, consumer):
+    consumer(path)
     w, s = make_weights(bits, N, K, seed=7 * N + K + bits)
     wn, sn = to_numpy_u8(w), to_numpy_u16(s)
     x = synthetic.activations(M, K, seed=N + 3 * M, outliers=True)
@@ -166,10 +182,11 @@ def test_gemv_matches_oracle(bits, M, N, K):
     assert ok, f"max err / tolerance = {worst}"
 
 
-@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("bits,path", BITS_PATHS)
 @pytest.mark.parametrize("M", [1, 3, 4])
 @pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (2048, 4096)])
-def test_fused_linear_matches_oracle_and_separate_path(bits, M, N, K):
+def test_fused_linear_matches_oracle_and_separate_path(bits, path, M, N, K, consumer):
+    consumer(path)
     w, s = make_weights(bits, N, K, seed=11 * N + K + bits)
     wn, sn = to_numpy_u8(w), to_numpy_u16(s)
     x = synthetic.activations(M, K, seed=5 * N + M, outliers=True)
@@ -188,7 +205,9 @@ def test_fused_linear_matches_oracle_and_separate_path(bits, M, N, K):
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
-def test_repeated_launches_are_bit_identical():
+@pytest.mark.parametrize("path", [DP4A, MMA])
+def test_repeated_launches_are_bit_identical(path, consumer):
+    consumer(path)
     bits, M, N, K = 4, 3, 4096, 4096
     w, s = make_weights(bits, N, K, seed=3)
     wdev = pack_host(bits, to_numpy_u8(w), to_numpy_u16(s), N, K)
@@ -213,8 +232,10 @@ def test_device_pack_matches_host_pack(bits, N, K):
     assert np.array_equal(dst.cpu().numpy(), host)
 
 
+@pytest.mark.parametrize("path", [DP4A, MMA])
 @pytest.mark.parametrize("cps,stages,pf", [(1, 2, 0), (1, 3, -1), (1, 4, 1024), (2, 2, -1), (2, 3, 64), (1, 8, -1)])
-def test_launch_configurations_agree(cps, stages, pf):
+def test_launch_configurations_agree(cps, stages, pf, path, consumer):
+    consumer(path)
     bits, M, N, K = 4, 2, 2048, 2048
     w, s = make_weights(bits, N, K, seed=21)
     wn, sn = to_numpy_u8(w), to_numpy_u16(s)
@@ -280,15 +301,22 @@ def test_empty_and_degenerate_shapes():
     assert woq.lib.woq_w4a8_linear_bf16(None, 0, None, 0, 8, 128, y0.data_ptr(), None, 0, None) == 0
     torch.cuda.synchronize()
     assert (y0.cpu().numpy() == 7.0).all()
-    # zero weights give exactly +0
+    # zero weights give exactly +0, with either int4 consumer
     N, K, M = 200, 256, 2
     packed = woq.woq_pack_w4(np.zeros((N, K // 2), np.uint8), np.full((N, 2), 0x3C00, np.uint16), N, K)
     x = synthetic.activations(M, K, seed=9).to(DEV)
-    y = run_linear(4, torch.from_numpy(packed).to(DEV), x, N, K, M)
-    assert not y.any() and not np.signbit(y).any()
+    for path in (DP4A, MMA):
+        woq.woq_tune_path(path)
+        try:
+            y = run_linear(4, torch.from_numpy(packed).to(DEV), x, N, K, M)
+        finally:
+            woq.woq_tune_path(0)
+        assert not y.any() and not np.signbit(y).any()
 
 
-def test_cuda_graph_replay_matches_eager():
+@pytest.mark.parametrize("path", [DP4A, MMA])
+def test_cuda_graph_replay_matches_eager(path, consumer):
+    consumer(path)
     bits, M, N, K = 4, 1, 4096, 4096
     w, s = make_weights(bits, N, K, seed=31)
     wdev = pack_host(bits, to_numpy_u8(w), to_numpy_u16(s), N, K)
@@ -319,14 +347,18 @@ def _sampled_rows(N, n_rand, seed):
     return np.array(sorted(r for r in rows if 0 <= r < N))
 
 
-@pytest.mark.parametrize("bits,M,K,N,fused", [
-    (4, 1, 5120, 152064, True),    # 27B LM head, decode
-    (4, 4, 17408, 5120, True),     # 27B down projection, MTP verification rows
-    (4, 3, 5120, 34816, False),    # 27B gate+up, int8 entry
-    (6, 4, 4096, 24576, True),     # 9B gate+up in W6
-    (6, 2, 12288, 4096, True),     # 9B down in W6
+@pytest.mark.parametrize("bits,M,K,N,fused,path", [
+    (4, 1, 5120, 152064, True, DP4A),   # 27B LM head, decode
+    (4, 1, 5120, 152064, True, MMA),
+    (4, 4, 17408, 5120, True, MMA),     # 27B down projection, MTP verification rows
+    (4, 4, 17408, 5120, True, DP4A),
+    (4, 3, 5120, 34816, False, MMA),    # 27B gate+up, int8 entry
+    (4, 2, 17408, 5120, False, MMA),    # 27B down, int8 entry (padded activation rows)
+    (6, 4, 4096, 24576, True, DP4A),    # 9B gate+up in W6
+    (6, 2, 12288, 4096, True, DP4A),    # 9B down in W6
 ])
-def test_full_size_sampled_rows(bits, M, K, N, fused):
+def test_full_size_sampled_rows(bits, M, K, N, fused, path, consumer):
+    consumer(path)
     seed = 100 + bits + M
     w, s = make_weights(bits, N, K, seed, device=DEV)
     wdev = torch.empty(woq.woq_packed_bytes(bits, N, K), dtype=torch.uint8, device=DEV)

@@ -3,7 +3,7 @@
 The byte positions are checked against the layout as documented in
 include/woq.h and the packer's layout notes (tile-major blocks of 128 rows x
 128 k; scales first, row 32j+l at half-word 4l+j; int4 chunk (c, j, l) at
-256 + 16 * ((4c + j) * 32 + l), word i holding k0 = 32c + 8i: low nibble of
+256 + 16 * ((4c + j) * 32 + (l ^ 2c)), word i holding k0 = 32c + 8i: low nibble of
 byte b = k0+b, high nibble = k0+4+b; int6 high bits in a second region).
 """
 import numpy as np
@@ -43,7 +43,7 @@ def test_header_fields():
     _, q, s = _rand(4, N, K, 1)
     packed = _pack(4, q, s, N, K)
     h = packed[:48].view(np.uint32)
-    assert h[0] == 0x31514F57 and h[1] == 1 and h[2] == 4 and h[3] == 128
+    assert h[0] == 0x31514F57 and h[1] == 2 and h[2] == 4 and h[3] == 128
     assert h[4] == N and h[5] == K and h[6] == 3 and h[7] == 3
     assert packed[8 * 4: 16 * 4].view(np.uint64).tolist()[:2] == [8448, woq.woq_packed_bytes(4, N, K)]
     assert not packed[48:256].any()
@@ -75,7 +75,7 @@ def test_documented_byte_positions(bits):
         # scale of (row, group)
         assert blk[:256].view(np.uint16)[4 * l + j] == s[n, g]
         # low four bits of the weight
-        byte = blk[256 + 16 * ((4 * c + j) * 32 + l) + 4 * i + b]
+        byte = blk[256 + 16 * ((4 * c + j) * 32 + (l ^ (2 * c))) + 4 * i + b]
         nib = (byte >> 4) if half else (byte & 0xF)
         assert nib == (wv[n, k] & 0xF)
         if bits == 6:
@@ -88,7 +88,7 @@ def test_documented_byte_positions(bits):
         j, l = divmod(r, 32)
         assert last[:256].view(np.uint16)[4 * l + j] == 0
         for c in range(4):
-            o = 256 + 16 * ((4 * c + j) * 32 + l)
+            o = 256 + 16 * ((4 * c + j) * 32 + (l ^ (2 * c)))
             assert not last[o: o + 16].any()
 
 

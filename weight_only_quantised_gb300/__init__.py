@@ -61,6 +61,7 @@ _SIGS = {
     "woq_debug_group_dots": ([_I, _P, _Z, _P, _I, _I, _I, _P, _P], _I),
     "woq_w4a8_linear_bf16_noalloc": ([_P, _Z, _P, _I, _I, _I, _P, _P], _I),
     "woq_tune_override": ([_I, _I, _I], _I),
+    "woq_tune_path": ([_I], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -223,3 +224,8 @@ def woq_debug_group_dots(bits: int, wpacked, q, N: int, K: int, dots, stream=Non
 
 def woq_tune_override(ctas_per_sm: int = 0, stages: int = 0, prefetch_kb: int = -1) -> None:
     _check(lib.woq_tune_override(ctas_per_sm, stages, prefetch_kb), "woq_tune_override")
+
+
+def woq_tune_path(path: int = 0) -> None:
+    """int4 consumer of later launches: 0 launch table, 1 dp4a, 2 tensor-core MMA."""
+    _check(lib.woq_tune_path(path), "woq_tune_path")

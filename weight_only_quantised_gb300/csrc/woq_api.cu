@@ -19,6 +19,7 @@ std::atomic<int> g_max_smem[kMaxDevices];
 std::atomic<int> g_override_cps{0};
 std::atomic<int> g_override_stages{0};
 std::atomic<int> g_override_prefetch_kb{-1};
+std::atomic<int> g_override_path{0};  // 0: table, else 1 + kern::Consumer
 std::atomic<int> g_launch_counter{0};  // numbers GEMV launches (trace builds key their stamps by it)
 
 int current_device() {
@@ -55,24 +56,38 @@ int max_dynamic_smem() {
 }
 
 // [barriers, flags, scratch: 512][reduction buffer][activations][ring]
-// activations: bf16 x quantised in place (fused, 2 M K bytes) or int8 q (M K bytes)
+// activations: bf16 x quantised in place (fused, 2 M K bytes) or int8 q (M rows); kernels
+// with tensor-core warps read q rows padded to K + 16 bytes (conflict-free fragment loads)
 static int red_bytes(int M) { return kStageBlocks * M * kTileRows * 4; }
 static constexpr int kMiscBytes = 512;
 static int act_offset(int M) { return kMiscBytes + red_bytes(M); }
-static int act_bytes(int M, int K, bool fused) { return (fused ? 2 : 1) * M * K; }
-static int ring_offset(int M, int K, bool fused) {
-  return (int)align_up((size_t)act_offset(M) + (size_t)act_bytes(M, K, fused), 128);
+static int act_stride(int K, int cons) { return cons != kern::kDp4a ? K + 16 : K; }
+static int act_bytes(int M, int K, bool fused, int cons) { return fused ? 2 * M * K : M * act_stride(K, cons); }
+static int ring_offset(int M, int K, bool fused, int cons) {
+  return (int)align_up((size_t)act_offset(M) + (size_t)act_bytes(M, K, fused, cons), 128);
+}
+
+// Consumer of the int4 kernels (kern::Consumer).  dp4a for every M <= 4: on this part the
+// f16 MMA (mma.sync, fp32 accumulate) costs about what dp4a costs at M = 4 and more below
+// it, and the two contend when mixed in one SM sub-partition.  The MMA's cost does not grow
+// with M; it stays selectable with woq_tune_path.  int6 is always dp4a.
+int choose_consumer(int bits, int M) {
+  (void)M;
+  if (bits != 4) return kern::kDp4a;
+  const int path = g_override_path.load(std::memory_order_relaxed);
+  if (path > 0) return path - 1;
+  return kern::kDp4a;
 }
 
 int smem_bytes_for(int bits, int M, int K, bool fused, int stages) {
-  return ring_offset(M, K, fused) + stages * kStageBlocks * block_bytes(bits);
+  return ring_offset(M, K, fused, choose_consumer(bits, M)) + stages * kStageBlocks * block_bytes(bits);
 }
 
 // Two CTAs (of this launch and the next) share an SM when each needs at most this much.
 static constexpr int kCoResidentBudget = (233472 - 2 * 1024) / 2;
 
 LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
-  LaunchConfig cfg = {0, 0, 0, 0};
+  LaunchConfig cfg = {0, 0, 0, 0, 0};
   const int sms = sm_count();
   const int smem_max = max_dynamic_smem();
   if (sms <= 0 || smem_max <= 0) return cfg;
@@ -111,6 +126,7 @@ LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
   cfg.stages = stages;
   cfg.smem_bytes = smem_bytes_for(bits, M, K, fused, stages);
   cfg.prefetch_stages = (int)(((long long)pf_kb * 1024 + stage_bytes - 1) / stage_bytes);
+  cfg.consumer = choose_consumer(bits, M);
   return cfg;
 }
 
@@ -131,7 +147,7 @@ using namespace woq;
 
 extern "C" {
 
-int woq_version(void) { return 100; }
+int woq_version(void) { return 200; }
 
 int woq_max_m(void) { return kMaxM; }
 
@@ -156,6 +172,12 @@ int woq_tune_override(int ctas_per_sm, int stages, int prefetch_kb) {
   g_override_cps.store(ctas_per_sm);
   g_override_stages.store(stages);
   g_override_prefetch_kb.store(prefetch_kb);
+  return WOQ_OK;
+}
+
+int woq_tune_path(int path) {
+  if (path < 0 || path > 2) return WOQ_ERR_SHAPE;
+  g_override_path.store(path);
   return WOQ_OK;
 }
 
@@ -254,11 +276,13 @@ static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_by
   p.NB = (uint32_t)nb64;
   p.stages = cfg.stages;
   p.prefetch_stages = cfg.prefetch_stages;
+  p.act_stride = act_stride(K, cfg.consumer);
   p.act_offset = act_offset(M);
   p.red_offset = kMiscBytes;
-  p.ring_offset = ring_offset(M, K, fused);
+  p.ring_offset = ring_offset(M, K, fused, cfg.consumer);
   p.launch_id = g_launch_counter.fetch_add(1, std::memory_order_relaxed) & 0x7fffffff;
-  const cudaError_t e = bits == 4 ? launch_gemv_w4(fused, M, p, cfg, stream) : launch_gemv_w6(fused, M, p, cfg, stream);
+  const cudaError_t e =
+      bits == 4 ? launch_gemv_w4(fused, cfg.consumer, M, p, cfg, stream) : launch_gemv_w6(fused, M, p, cfg, stream);
   return e == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
 }
 

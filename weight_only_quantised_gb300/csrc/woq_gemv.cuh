@@ -66,6 +66,7 @@ struct GemvParams {
   uint32_t NB;              // T * G blocks; (grid + 1) * NB < 2^32, so partition math stays 32-bit
   int stages;               // shared-memory ring stages
   int prefetch_stages;      // stages' worth of weights kept in flight into L2 beyond the ring
+  int act_stride;           // bytes between activation rows of q in shared memory (K, or K + 16)
   int act_offset;           // shared-memory offsets (bytes)
   int red_offset;
   int ring_offset;
@@ -160,10 +161,11 @@ __device__ __forceinline__ void unpack_word(uint32_t v, uint32_t uh, int e, uint
 // acc[jj][m] += term(row 32(2h+jj)+lane, m).  The int4 (or int6) lanes of the low and
 // high nibbles accumulate into separate int32 chains (more independent dp4a), summed
 // exactly at the end of the group.
-template <int BITS, int M>
+template <int BITS, int M, int R, int C>
 __device__ __forceinline__ void consume_half_block(const uint8_t* __restrict__ blk, const int8_t* __restrict__ act,
-                                                   int K, int g, int lane, int h, const float (&as)[M],
-                                                   float (&acc)[2][M]) {
+                                                   int qs, int g, int lane, int h, const float (&as)[M],
+                                                   float (&acc)[R][C]) {
+  static_assert(R >= 2 && C >= M, "accumulators [2][M] (or a wider array)");
   const uint2 sc = *reinterpret_cast<const uint2*>(blk + 8 * lane);
   const uint32_t sw = h ? sc.y : sc.x;  // scales of rows 32(2h) + lane and 32(2h+1) + lane
   float wsc[2];
@@ -184,15 +186,15 @@ __device__ __forceinline__ void consume_half_block(const uint8_t* __restrict__ b
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
       const int j = 2 * h + jj;
-      v[jj] = *reinterpret_cast<const uint4*>(blk + kScaleBytes + ((c * 4 + j) * 32 + lane) * 16);
+      v[jj] = *reinterpret_cast<const uint4*>(blk + w4_chunk_offset(c, j, lane));
       if constexpr (BITS == 6)
-        u[jj] = *reinterpret_cast<const uint2*>(blk + kScaleBytes + kW4Bytes + ((c * 4 + j) * 32 + lane) * 8);
+        u[jj] = *reinterpret_cast<const uint2*>(blk + hi_chunk_offset(c, j, lane));
     }
     uint32_t a[M][8];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      const uint4 a0 = *reinterpret_cast<const uint4*>(ag + (size_t)m * K + 32 * c);
-      const uint4 a1 = *reinterpret_cast<const uint4*>(ag + (size_t)m * K + 32 * c + 16);
+      const uint4 a0 = *reinterpret_cast<const uint4*>(ag + m * qs + 32 * c);
+      const uint4 a1 = *reinterpret_cast<const uint4*>(ag + m * qs + 32 * c + 16);
       a[m][0] = a0.x; a[m][1] = a0.y; a[m][2] = a0.z; a[m][3] = a0.w;
       a[m][4] = a1.x; a[m][5] = a1.y; a[m][6] = a1.z; a[m][7] = a1.w;
     }
@@ -220,6 +222,133 @@ __device__ __forceinline__ void consume_half_block(const uint8_t* __restrict__ b
       const float t = __fmul_rn(__fmul_rn(dev::small_int_to_float(dlo[jj][m] + dhi[jj][m]), wsc[jj]), as[m]);
       acc[jj][m] = __fadd_rn(acc[jj][m], t);
     }
+}
+
+// ---------------------------------------------------------------------------------------
+// Tensor-core consumer (int4): one half block by one warp with the f16 MMA
+// mma.sync m16n8k16 (fp32 accumulate).  Lane L = 4g + t.  The warp's 64 rows are four
+// 16-row m-tiles; in m-tile mt lane L supplies rows 16mt + g and 16mt + g + 8, 32-k
+// quarter t of the group (one 16-byte chunk per row).  Word i of a chunk (k0 = 32t + 8i)
+// feeds two MMAs, one for its low nibbles (k0 .. k0+3), one for its high nibbles
+// (k0+4 .. k0+7), with A elements made by a single LOP3 each:
+//   low:  f16(1024 + (w + 8))       high: f16(1024 + 16 (w + 8))
+// (the nibble's top bit flipped gives w + 8 in [0, 15]).  B is q of activation row g
+// (zero for g >= M) at the same k, converted to f16 exactly.  Products and every partial
+// sum are integers below 2^24, so the fp32 accumulators are exact whatever order the
+// tensor core adds in.  With S_lo and S_hi the sums of q over the group's low- and
+// high-nibble positions,
+//   d = acc_lo + acc_hi / 16 - (1032 S_lo + 72 S_hi) = sum_k w q
+// exactly (every intermediate below 9.2e6 < 2^24).  acc[mt][v] accumulates d * wscale over
+// the groups for (row g + 8 (v >> 1), column 2t + (v & 1)) of m-tile mt; the caller
+// applies the activation scale.
+__device__ __forceinline__ uint32_t lop3_sel_xor(uint32_t a, uint32_t mask, uint32_t c) {
+  uint32_t d;  // mask ? a ^ c : c
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(mask), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// int8 q bytes (q0, q1, q2, q3) -> f16x2 (q0, q2) and (q1, q3), exact
+__device__ __forceinline__ void q4_to_f16x2(uint32_t q4, uint32_t& b02, uint32_t& b13) {
+  const uint32_t u = q4 ^ 0x80808080u;  // q + 128 per byte
+  uint32_t r02 = __byte_perm(u, 0x64646464u, 0x4240);  // f16 1024 + q + 128
+  uint32_t r13 = __byte_perm(u, 0x64646464u, 0x4341);
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r02) : "r"(0x64806480u));  // - 1152
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r13) : "r"(0x64806480u));
+  b02 = r02;
+  b13 = r13;
+}
+
+template <int M>
+__device__ __forceinline__ void consume_half_block_mma(const uint8_t* __restrict__ blk, const int8_t* __restrict__ act,
+                                                       int qs, int g_idx, int lane, int h, float (&acc)[4][4]) {
+  const int g = lane >> 2, t = lane & 3;
+  // B fragments and the group's offset correction for activation row g
+  uint32_t bl0[4], bl1[4], bh0[4], bh1[4];
+  int corr = 0;
+  if (g < M) {
+    const int8_t* ap = act + g * qs + g_idx * kGroup + 32 * t;
+    const uint4 qa = *reinterpret_cast<const uint4*>(ap);
+    const uint4 qb = *reinterpret_cast<const uint4*>(ap + 16);
+    const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    int s_lo = 0, s_hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      q4_to_f16x2(qw[2 * i], bl0[i], bl1[i]);
+      q4_to_f16x2(qw[2 * i + 1], bh0[i], bh1[i]);
+      s_lo = dev::dp4a_ss(qw[2 * i], 0x01010101u, s_lo);
+      s_hi = dev::dp4a_ss(qw[2 * i + 1], 0x01010101u, s_hi);
+    }
+    corr = 1032 * s_lo + 72 * s_hi;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bl0[i] = bl1[i] = bh0[i] = bh1[i] = 0u;
+  }
+  corr += __shfl_xor_sync(0xffffffffu, corr, 1);
+  corr += __shfl_xor_sync(0xffffffffu, corr, 2);
+  // columns 2t, 2t+1 of D are activation rows 2t, 2t+1: their corrections
+  const float c0 = -(float)__shfl_sync(0xffffffffu, corr, 8 * t);
+  const float c1 = -(float)__shfl_sync(0xffffffffu, corr, 8 * t + 4);
+
+  // fp16 weight scales of rows 16mt + g + 8s: word [mt & 1][s] holds m-tiles (mt & 1, (mt & 1) + 2)
+  // as its (low, high) halves
+  uint32_t sw[2][2];
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      sw[p][s] = *reinterpret_cast<const uint32_t*>(blk + 2 * (scale_index(16 * p + 8 * s + g) + 2 * h));
+
+  const int gx = g ^ (2 * t);
+  // two m-tiles at a time: four independent accumulator chains per warp
+#pragma unroll
+  for (int mp = 0; mp < 2; ++mp) {
+    const uint8_t* base = blk + kScaleBytes + ((4 * t + 2 * h + mp) * 32 + gx) * 16;
+    uint32_t wa[2][4], wb[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {  // m-tile 2mp + u: rows 16(2mp+u) + g (+8) sit at lane slot 16u + gx (+8)
+      const uint4 va = *reinterpret_cast<const uint4*>(base + (16 * u) * 16);
+      const uint4 vb = *reinterpret_cast<const uint4*>(base + (16 * u + 8) * 16);
+      wa[u][0] = va.x; wa[u][1] = va.y; wa[u][2] = va.z; wa[u][3] = va.w;
+      wb[u][0] = vb.x; wb[u][1] = vb.y; wb[u][2] = vb.z; wb[u][3] = vb.w;
+    }
+    float dl[2][4], dh[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) dl[u][v] = dh[u][v] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t a = wa[u][i], b = wb[u][i], sa = a >> 8, sb = b >> 8;
+        mma_16816(dl[u], lop3_sel_xor(a, 0x000F000Fu, 0x64086408u), lop3_sel_xor(b, 0x000F000Fu, 0x64086408u),
+                  lop3_sel_xor(sa, 0x000F000Fu, 0x64086408u), lop3_sel_xor(sb, 0x000F000Fu, 0x64086408u), bl0[i],
+                  bl1[i]);
+        mma_16816(dh[u], lop3_sel_xor(a, 0x00F000F0u, 0x64806480u), lop3_sel_xor(b, 0x00F000F0u, 0x64806480u),
+                  lop3_sel_xor(sa, 0x00F000F0u, 0x64806480u), lop3_sel_xor(sb, 0x00F000F0u, 0x64806480u), bh0[i],
+                  bh1[i]);
+      }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int mt = 2 * mp + u;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        // acc_lo + acc_hi / 16 (<= 9.1e6) and the correction are exact, so d is the exact group dot
+        const float d = __fadd_rn(__fmaf_rn(dh[u][v], 0.0625f, dl[u][v]), (v & 1) ? c1 : c0);
+        const uint32_t w2 = sw[u][v >> 1];
+        const float ws = dev::half_bits_to_float(mp == 0 ? (w2 & 0xFFFFu) : (w2 >> 16));
+        acc[mt][v] = __fmaf_rn(d, ws, acc[mt][v]);
+      }
+    }
+  }
 }
 
 // The blocks of one CTA's range, as work items (tile t, groups [ga, gb)) in processing
@@ -284,8 +413,8 @@ struct StageCursor {
 
 // Activation prologue of the fused entry, run by the consumer warps on the bf16 x
 // that one bulk copy placed at act[0, 2 M K): per-row amax, scale = amax / 127, and
-// q = rne(x / scale) written in place over the first M K bytes (q byte e overwrites
-// only x bytes of values with index <= e).
+// q = rne(x / scale) written in place, row m at act + m qs (qs = K or K + 16 <= 2K, so
+// the q byte of value e overwrites only x bytes of values with index <= e).
 //
 // Rows with K <= kConsumers * 8 * (kRegVecs / M) are read once into registers; the
 // barrier after the amax pass then guarantees that every x value has been read
@@ -386,8 +515,8 @@ __device__ __forceinline__ uint32_t row_gate(float sc, float rc) {
 }
 
 template <int M>
-__device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, int lane, int warp, float* s_scratch,
-                                                  float* s_as, int launch_id) {
+__device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, int tid, int lane, int warp,
+                                                  float* s_scratch, float* s_as, int launch_id) {
   constexpr int kVPR = kRegVecs / M;  // vectors per row held in registers
   constexpr int kStride = kConsumers * 8;  // values per vector round of all threads
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
@@ -426,7 +555,7 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, 
         uint32_t g = gate;
         const uint2 q = quantise8_fast(xv[m][j], rc2, g);
         if (k < K) {
-          *reinterpret_cast<uint2*>(act + m * K + k) = sc[m] == 0.0f ? make_uint2(0u, 0u) : q;
+          *reinterpret_cast<uint2*>(act + m * qs + k) = sc[m] == 0.0f ? make_uint2(0u, 0u) : q;
           if (!(g >> 31) && sc[m] != 0.0f) redo |= 1u << (m * kVPR + j);
         }
       }
@@ -437,7 +566,7 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, 
 #pragma unroll
         for (int j = 0; j < kVPR; ++j)
           if (redo & (1u << (m * kVPR + j)))
-            *reinterpret_cast<uint2*>(act + m * K + 8 * tid + kStride * j) = quantise8_exact(xv[m][j], sc[m]);
+            *reinterpret_cast<uint2*>(act + m * qs + 8 * tid + kStride * j) = quantise8_exact(xv[m][j], sc[m]);
     }
     return;
   }
@@ -476,7 +605,7 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, 
         uint32_t g = gate;
         const uint2 q = quantise8_fast(xv[v], rc2, g);
         if (k < K) {
-          *reinterpret_cast<uint2*>(act + m * K + k) = sc[m] == 0.0f ? make_uint2(0u, 0u) : q;
+          *reinterpret_cast<uint2*>(act + m * qs + k) = sc[m] == 0.0f ? make_uint2(0u, 0u) : q;
           if (!(g >> 31) && sc[m] != 0.0f) redo |= 1u << v;
         }
       }
@@ -484,14 +613,19 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int tid, 
 #pragma unroll
         for (int v = 0; v < 4; ++v)
           if (redo & (1u << v))
-            *reinterpret_cast<uint2*>(act + m * K + k0 + 8 * tid + kStride * v) = quantise8_exact(xv[v], sc[m]);
+            *reinterpret_cast<uint2*>(act + m * qs + k0 + 8 * tid + kStride * v) = quantise8_exact(xv[v], sc[m]);
       }
     }
   }
 }
 
-template <int BITS, int M, bool FUSED>
-__global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvParams p) {
+// Consumer of a kernel instance: every consumer warp on dp4a, or every one on the f16
+// tensor-core MMA.
+enum Consumer { kDp4a = 0, kMma = 1 };
+
+template <int BITS, int M, bool FUSED, int CONS>
+__global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 288 threads x 112 fit one SM
+  static_assert(CONS == kDp4a || BITS == 4, "the tensor-core consumer reads int4 blocks");
   constexpr int BB = Fmt<BITS>::kBlockBytes;
   constexpr int kStageBytes = kSB * BB;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -621,7 +755,12 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
     WOQ_TRACE_EV(3);
     const uint32_t act_bytes = (uint32_t)(FUSED ? 2 * M * p.K : M * p.K);
     dev::mbar_arrive_expect_tx(actbar, act_bytes);
-    dev::bulk_copy_g2s(act, FUSED ? static_cast<const void*>(p.x) : static_cast<const void*>(p.q), act_bytes, actbar);
+    if (FUSED || p.act_stride == p.K) {
+      dev::bulk_copy_g2s(act, FUSED ? static_cast<const void*>(p.x) : static_cast<const void*>(p.q), act_bytes, actbar);
+    } else {
+      for (int m = 0; m < M; ++m)
+        dev::bulk_copy_g2s(act + m * p.act_stride, p.q + (size_t)m * p.K, (uint32_t)p.K, actbar);
+    }
     hdr0 = *reinterpret_cast<const uint4*>(p.w);
     hdr1 = *reinterpret_cast<const uint4*>(p.w + 16);
   }
@@ -645,7 +784,7 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
     }
   }
   if constexpr (FUSED) {
-    quantise_prologue<M>(act, p.K, tid, lane, warp, s_scratch, s_as, p.launch_id);
+    quantise_prologue<M>(act, p.K, p.act_stride, tid, lane, warp, s_scratch, s_as, p.launch_id);
   } else {
     if (tid < M) s_as[tid] = ascale_in;
   }
@@ -671,15 +810,18 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
     int ga, gb;
     order.get(item, t, ga, gb);
 
-    float acc[2][M];
+    // dp4a: [row half][m]; MMA: [m-tile][fragment]
+    constexpr int kAccR = CONS == kDp4a ? 2 : 4, kAccC = CONS == kDp4a ? M : 4;
+    float acc[kAccR][kAccC];
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj)
+    for (int jj = 0; jj < kAccR; ++jj)
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[jj][m] = 0.0f;
+      for (int m = 0; m < kAccC; ++m) acc[jj][m] = 0.0f;
 
     for (int g0 = ga; g0 < gb; g0 += kSB) {
       const int nb = gb - g0 < kSB ? gb - g0 : kSB;
-      if (!aborted && !dev::mbar_wait_bounded(full + slot, phase)) {
+      // (the verdict is made warp-uniform: the tensor-core consumer shuffles across the warp)
+      if (!aborted && !__all_sync(0xffffffffu, dev::mbar_wait_bounded(full + slot, phase))) {
         aborted = true;
         s_flags[1] = 1;
         atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
@@ -690,9 +832,14 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
       if (tid == 0 && n_stage < 16) WOQ_TRACE_EV(16 + n_stage);
       ++n_stage;
 #endif
-      if (!aborted && hb < nb)
-        consume_half_block<BITS, M>(ring + (size_t)slot * kStageBytes + (size_t)hb * BB, actq, p.K, g0 + hb, lane, hh,
-                                    as, acc);
+      if (!aborted && hb < nb) {
+        const uint8_t* blk = ring + (size_t)slot * kStageBytes + (size_t)hb * BB;
+        if constexpr (CONS == kDp4a) {
+          consume_half_block<BITS, M>(blk, actq, p.act_stride, g0 + hb, lane, hh, as, acc);
+        } else {
+          consume_half_block_mma<M>(blk, actq, p.act_stride, g0 + hb, lane, hh, acc);
+        }
+      }
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(empty + slot);
       if (++slot == stages) {
@@ -702,10 +849,25 @@ __global__ void __launch_bounds__(kConsumers + 32, 2) gemv_kernel(const GemvPara
     }
 
     // reduce the four blocks' partial sums for this tile: red[block][m][row]
+    if constexpr (CONS == kMma) {
+      // MMA sums are sum_g d * wscale; the activation scale of columns 2t, 2t+1 is applied here
+      const int g = lane >> 2, t2 = 2 * (lane & 3);
+      const float a0 = s_as[t2 < M ? t2 : M - 1], a1 = s_as[t2 + 1 < M ? t2 + 1 : M - 1];
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj)
+      for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-      for (int m = 0; m < M; ++m) red[(hb * M + m) * kTileRows + 64 * hh + 32 * jj + lane] = acc[jj][m];
+        for (int v = 0; v < 4; ++v) {
+          const int m = t2 + (v & 1);
+          if (m < M)
+            red[(hb * M + m) * kTileRows + 64 * hh + 16 * mt + g + 8 * (v >> 1)] =
+                __fmul_rn(acc[mt][v], (v & 1) ? a1 : a0);
+        }
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int m = 0; m < M; ++m) red[(hb * M + m) * kTileRows + 64 * hh + 32 * jj + lane] = acc[jj][m];
+    }
     dev::named_barrier_sync(kBarConsumers, kConsumers);
     const bool write_ok = header_ok && s_flags[1] == 0;
     const int row = tid & (kTileRows - 1);

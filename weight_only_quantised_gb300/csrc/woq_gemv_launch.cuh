@@ -8,9 +8,9 @@
 
 namespace woq {
 
-template <int BITS, int M, bool FUSED>
+template <int BITS, int M, bool FUSED, int CONS>
 cudaError_t launch_gemv_instance(const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream) {
-  auto kernel = kern::gemv_kernel<BITS, M, FUSED>;
+  auto kernel = kern::gemv_kernel<BITS, M, FUSED, CONS>;
   // raise the kernel's dynamic shared-memory limit once per device
   static std::atomic<unsigned long long> configured{0};
   int device = 0;
@@ -35,23 +35,27 @@ cudaError_t launch_gemv_instance(const GemvParams& p, const LaunchConfig& cfg, c
   return cudaLaunchKernelEx(&lc, kernel, p);
 }
 
-template <int BITS, bool FUSED>
+template <int BITS, bool FUSED, int CONS>
 cudaError_t launch_gemv_m(int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream) {
   switch (M) {
-    case 1: return launch_gemv_instance<BITS, 1, FUSED>(p, cfg, stream);
-    case 2: return launch_gemv_instance<BITS, 2, FUSED>(p, cfg, stream);
-    case 3: return launch_gemv_instance<BITS, 3, FUSED>(p, cfg, stream);
-    case 4: return launch_gemv_instance<BITS, 4, FUSED>(p, cfg, stream);
+    case 1: return launch_gemv_instance<BITS, 1, FUSED, CONS>(p, cfg, stream);
+    case 2: return launch_gemv_instance<BITS, 2, FUSED, CONS>(p, cfg, stream);
+    case 3: return launch_gemv_instance<BITS, 3, FUSED, CONS>(p, cfg, stream);
+    case 4: return launch_gemv_instance<BITS, 4, FUSED, CONS>(p, cfg, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int BITS>
+template <int BITS, int CONS>
 cudaError_t launch_gemv_bits(bool fused, int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream) {
-  return fused ? launch_gemv_m<BITS, true>(M, p, cfg, stream) : launch_gemv_m<BITS, false>(M, p, cfg, stream);
+  return fused ? launch_gemv_m<BITS, true, CONS>(M, p, cfg, stream) : launch_gemv_m<BITS, false, CONS>(M, p, cfg, stream);
 }
 
-cudaError_t launch_gemv_w4(bool fused, int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream);
+// cons: kern::Consumer of the launch (int4 only; int6 is always dp4a)
+cudaError_t launch_gemv_w4(bool fused, int cons, int M, const GemvParams& p, const LaunchConfig& cfg,
+                           cudaStream_t stream);
+cudaError_t launch_gemv_w4_mma(bool fused, int cons, int M, const GemvParams& p, const LaunchConfig& cfg,
+                               cudaStream_t stream);
 cudaError_t launch_gemv_w6(bool fused, int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream);
 
 }  // namespace woq

@@ -1,10 +1,12 @@
-// Instantiations of the skinny GEMV / linear kernel for int4 weights.
+// Instantiations of the skinny GEMV / linear kernel for int4 weights (dp4a consumer).
 #include "woq_gemv_launch.cuh"
 
 namespace woq {
 
-cudaError_t launch_gemv_w4(bool fused, int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream) {
-  return launch_gemv_bits<4>(fused, M, p, cfg, stream);
+cudaError_t launch_gemv_w4(bool fused, int cons, int M, const GemvParams& p, const LaunchConfig& cfg,
+                           cudaStream_t stream) {
+  if (cons != kern::kDp4a) return launch_gemv_w4_mma(fused, cons, M, p, cfg, stream);
+  return launch_gemv_bits<4, kern::kDp4a>(fused, M, p, cfg, stream);
 }
 
 }  // namespace woq

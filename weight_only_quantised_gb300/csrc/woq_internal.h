@@ -17,6 +17,7 @@ struct LaunchConfig {
   int stages;           // ring stages of kStageBlocks blocks each
   int smem_bytes;       // dynamic shared memory per CTA
   int prefetch_stages;  // stages kept in flight into L2 beyond the ring
+  int consumer;         // kern::Consumer (dp4a or tensor-core MMA)
 };
 
 // Workspace layout: [status word + pad: 256 B][tagged partial sums: ctas x 2 x M x 128 x 8 B]
@@ -32,6 +33,7 @@ constexpr int kMaxStages = 8;
 
 int sm_count();                       // SMs of the current device (cached per device)
 int max_dynamic_smem();               // opt-in shared memory per block of the current device
+int choose_consumer(int bits, int M);  // kern::Consumer the launch table picks for (bits, M)
 int smem_bytes_for(int bits, int M, int K, bool fused, int stages);
 LaunchConfig choose_config(int bits, int M, int N, int K, bool fused);
 WorkspaceLayout workspace_layout(int M, int N, int ctas);

@@ -20,8 +20,11 @@
 //   bytes [0, 256)     fp16 scales; row 32j+l at half-word index 4l + j, so lane
 //                      l reads its four scales with one 8-byte load.
 //   bytes [256, 8448)  int4 weights: 16 chunks (c, j), c = 0..3 the 32-k quarter
-//                      of the group, each chunk 32 lanes x 16 bytes (lane l at
-//                      byte 16l: consecutive lanes read consecutive 16 bytes).
+//                      of the group, each chunk 32 lanes x 16 bytes, lane l at
+//                      byte 16 (l ^ 2c).  The swizzle keeps both consumer patterns
+//                      free of shared-memory bank conflicts: 32 consecutive rows of
+//                      one quarter (the dp4a path), and rows {g, g+8} x quarters
+//                      {0..3} (the tensor-core path, lane 4g + t reading quarter t).
 //                      The 16 bytes of (c, j, l) hold row 32j+l, k = 32c .. 32c+31
 //                      as four 32-bit words; word i holds k0 = 32c + 8i .. k0+7:
 //                      byte b has k0+b in its low nibble and k0+4+b in its high
@@ -53,7 +56,7 @@
 namespace woq {
 
 constexpr uint32_t kMagic = 0x31514F57u;  // "WOQ1" little-endian
-constexpr uint32_t kLayoutVersion = 1;
+constexpr uint32_t kLayoutVersion = 2;
 constexpr int kHeaderBytes = 256;
 constexpr int kTileRows = 128;
 constexpr int kGroup = 128;
@@ -90,7 +93,9 @@ inline size_t packed_bytes(int bits, long N, long K) {
 }
 
 // Byte offset, inside a block, of the 16-byte int4 chunk of quarter c, row group j, lane l.
-WOQ_HD inline constexpr int w4_chunk_offset(int c, int j, int l) { return kScaleBytes + ((c * 4 + j) * 32 + l) * 16; }
+WOQ_HD inline constexpr int w4_chunk_offset(int c, int j, int l) {
+  return kScaleBytes + ((c * 4 + j) * 32 + (l ^ (2 * c))) * 16;
+}
 // Byte offset, inside a block, of the 8-byte high-bit chunk of quarter c, row group j, lane l (int6).
 WOQ_HD inline constexpr int hi_chunk_offset(int c, int j, int l) { return kScaleBytes + kW4Bytes + ((c * 4 + j) * 32 + l) * 8; }
 // Half-word index, inside a block's scale area, of row r.

@@ -93,10 +93,10 @@ __global__ void group_dots_kernel(const uint8_t* __restrict__ w, const int8_t* _
 #pragma unroll
     for (int m = 0; m < M; ++m) d[m] = 0;
     for (int c = 0; c < 4; ++c) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(blk + kScaleBytes + ((c * 4 + j) * 32 + l) * 16));
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(blk + w4_chunk_offset(c, j, l)));
       uint2 u = make_uint2(0u, 0u);
       if constexpr (BITS == 6)
-        u = __ldg(reinterpret_cast<const uint2*>(blk + kScaleBytes + kW4Bytes + ((c * 4 + j) * 32 + l) * 8));
+        u = __ldg(reinterpret_cast<const uint2*>(blk + hi_chunk_offset(c, j, l)));
       const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -182,9 +182,9 @@ __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __res
           }
         }
     }
-    *reinterpret_cast<uint4*>(blk + kScaleBytes + ((c * 4 + j) * 32 + l) * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(blk + w4_chunk_offset(c, j, l)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     if constexpr (BITS == 6)
-      *reinterpret_cast<uint2*>(blk + kScaleBytes + kW4Bytes + ((c * 4 + j) * 32 + l) * 8) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(blk + hi_chunk_offset(c, j, l)) = make_uint2(hi[0], hi[1]);
     if (c == 0) {
       const int r = 32 * j + l;
       const uint16_t s = n < N ? scales[(size_t)n * G + g] : (uint16_t)0;
