@@ -57,14 +57,26 @@ int max_dynamic_smem() {
 
 // [barriers, flags, scratch: 512][reduction buffer][activations][ring]
 // activations: bf16 x quantised in place (fused, 2 M K bytes) or int8 q (M rows); kernels
-// with tensor-core warps read q rows padded to K + 16 bytes (conflict-free fragment loads)
+// with tensor-core warps read q rows padded to K + 16 bytes (conflict-free fragment loads).
+// In the fused entry q needs only the first M (K or K + 16) bytes once the prologue is
+// done, and the reduction buffer is first written after it, so when the bf16 tail is
+// large enough the reduction buffer lives there: [512][activations (q + reduction)][ring].
 static int red_bytes(int M) { return kStageBlocks * M * kTileRows * 4; }
 static constexpr int kMiscBytes = 512;
-static int act_offset(int M) { return kMiscBytes + red_bytes(M); }
 static int act_stride(int K, int cons) { return cons != kern::kDp4a ? K + 16 : K; }
 static int act_bytes(int M, int K, bool fused, int cons) { return fused ? 2 * M * K : M * act_stride(K, cons); }
+static int q_end(int M, int K, int cons) { return (int)align_up((size_t)M * act_stride(K, cons), 16); }
+static bool red_in_act(int M, int K, bool fused, int cons) {
+  return fused && q_end(M, K, cons) + red_bytes(M) <= act_bytes(M, K, fused, cons);
+}
+static int act_offset(int M, int K, bool fused, int cons) {
+  return kMiscBytes + (red_in_act(M, K, fused, cons) ? 0 : red_bytes(M));
+}
+static int red_offset(int M, int K, bool fused, int cons) {
+  return red_in_act(M, K, fused, cons) ? act_offset(M, K, fused, cons) + q_end(M, K, cons) : kMiscBytes;
+}
 static int ring_offset(int M, int K, bool fused, int cons) {
-  return (int)align_up((size_t)act_offset(M) + (size_t)act_bytes(M, K, fused, cons), 128);
+  return (int)align_up((size_t)act_offset(M, K, fused, cons) + (size_t)act_bytes(M, K, fused, cons), 128);
 }
 
 // Consumer of the int4 kernels (kern::Consumer).  dp4a for every M <= 4: on this part the
@@ -277,8 +289,8 @@ static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_by
   p.stages = cfg.stages;
   p.prefetch_stages = cfg.prefetch_stages;
   p.act_stride = act_stride(K, cfg.consumer);
-  p.act_offset = act_offset(M);
-  p.red_offset = kMiscBytes;
+  p.act_offset = act_offset(M, K, fused, cfg.consumer);
+  p.red_offset = red_offset(M, K, fused, cfg.consumer);
   p.ring_offset = ring_offset(M, K, fused, cfg.consumer);
   p.launch_id = g_launch_counter.fetch_add(1, std::memory_order_relaxed) & 0x7fffffff;
   const cudaError_t e =

@@ -416,19 +416,24 @@ struct StageCursor {
 // q = rne(x / scale) written in place, row m at act + m qs (qs = K or K + 16 <= 2K, so
 // the q byte of value e overwrites only x bytes of values with index <= e).
 //
+// The amax covers the whole row; q is only formed for k in [klo1, khi1) and [klo2, khi2),
+// the groups this CTA's blocks read (the rest of the tile is never looked at).
+//
 // Rows with K <= kConsumers * 8 * (kRegVecs / M) are read once into registers; the
 // barrier after the amax pass then guarantees that every x value has been read
 // before any q byte is written.  Longer rows are quantised in rounds, each read in
-// full before any thread of the round writes.  Every vector is stored as the fast
-// route gives it; one warp vote afterwards sends the rare vectors with a quotient
-// near a tie through the exact route, which stores them again.
+// full before any thread of the round writes (the amax pass has read everything
+// before the first write, so skipped rounds need no reads).  Every vector is stored
+// as the fast route gives it; one warp vote afterwards sends the rare vectors with a
+// quotient near a tie through the exact route, which stores them again.
 constexpr int kRegVecs = 12;  // 8-value vectors per thread kept in registers
 
 // Row scale s = RN(amax / 127) and rc = RN(1 / s) for a bf16 amax held in an fp32.
 // For 2^-119 <= amax < inf, amax = A 2^e with A = 1 + f/128 and the significand
 // tables hold RN(A / 127) and RN(1 / RN(A / 127)); a power of two passes through
 // round-to-nearest unchanged while the result stays normal, so both are exact.
-// Zero, tiny and non-finite amax take the IEEE division and reciprocal.
+// An all-zero row gets s = 0 and rc = 0 (the fast route then yields q = 0); tiny and
+// non-finite amax take the IEEE division and reciprocal.
 __device__ __forceinline__ void scale_and_rcp(float amax, float& s, float& rc) {
   const uint32_t b = __float_as_uint(amax);
   const uint32_t e = b >> 23;  // biased exponent (amax >= 0)
@@ -437,6 +442,9 @@ __device__ __forceinline__ void scale_and_rcp(float amax, float& s, float& rc) {
     const uint32_t sh = (e - 127u) << 23;  // two's complement exponent shift
     s = __uint_as_float(kScaleSig[f] + sh);
     rc = __uint_as_float(kRcpSig[f] - sh);
+  } else if (amax == 0.0f) {
+    s = 0.0f;   // all-zero row: q = 0
+    rc = 0.0f;  // so that the fast route gives t = 0, q = 0, far from any tie
   } else {
     s = __fdiv_rn(amax, 127.0f);
     rc = __frcp_rn(s);
@@ -508,15 +516,14 @@ __device__ __forceinline__ void row_scales(const float (&lmax)[M], int tid, int 
   }
 }
 
-// Fast-route gate of a row: all ones when the fast route may decide (rc finite, or an
-// all-zero row, stored as zeros), else zero so that every vector of the row is redone.
-__device__ __forceinline__ uint32_t row_gate(float sc, float rc) {
-  return (sc == 0.0f || rc <= 3.4028234e38f) ? 0xFFFFFFFFu : 0u;
-}
+// Fast-route gate of a row: all ones when the fast route may decide (rc finite; an
+// all-zero row has rc = 0), else zero so that every vector of the row is redone.
+__device__ __forceinline__ uint32_t row_gate(float rc) { return rc <= 3.4028234e38f ? 0xFFFFFFFFu : 0u; }
 
 template <int M>
-__device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, int tid, int lane, int warp,
-                                                  float* s_scratch, float* s_as, int launch_id) {
+__device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, int klo1, int khi1, int klo2, int khi2,
+                                                  int tid, int lane, int warp, float* s_scratch, float* s_as,
+                                                  int launch_id) {
   constexpr int kVPR = kRegVecs / M;  // vectors per row held in registers
   constexpr int kStride = kConsumers * 8;  // values per vector round of all threads
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
@@ -543,20 +550,24 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
     }
     row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
     if (tid == 0) WOQ_TRACE_EV2(5);
-    uint32_t redo = 0;  // bit m * kVPR + j
+    dev::f32x2 rc2[M];
+    uint32_t gate[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      const dev::f32x2 rc2 = dev::f2_splat(rc[m]);
-      const uint32_t gate = row_gate(sc[m], rc[m]);
+      rc2[m] = dev::f2_splat(rc[m]);
+      gate[m] = row_gate(rc[m]);
+    }
+    uint32_t redo = 0;  // bit m * kVPR + j
 #pragma unroll
-      for (int j = 0; j < kVPR; ++j) {
-        if (kStride * j >= K) break;
-        const int k = 8 * tid + kStride * j;
-        uint32_t g = gate;
-        const uint2 q = quantise8_fast(xv[m][j], rc2, g);
-        if (k < K) {
-          *reinterpret_cast<uint2*>(act + m * qs + k) = sc[m] == 0.0f ? make_uint2(0u, 0u) : q;
-          if (!(g >> 31) && sc[m] != 0.0f) redo |= 1u << (m * kVPR + j);
+    for (int j = 0; j < kVPR; ++j) {
+      if (kStride * j >= K) break;  // uniform
+      const int k = 8 * tid + kStride * j;
+      if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {  // read by this CTA
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          uint32_t g = gate[m];
+          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(xv[m][j], rc2[m], g);
+          redo |= (~g >> 31) << (m * kVPR + j);
         }
       }
     }
@@ -589,8 +600,10 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
 #pragma unroll
   for (int m = 0; m < M; ++m) {
     const dev::f32x2 rc2 = dev::f2_splat(rc[m]);
-    const uint32_t gate = row_gate(sc[m], rc[m]);
+    const uint32_t gate = row_gate(rc[m]);
     for (int k0 = 0; k0 < K; k0 += 4 * kStride) {
+      // CTA-uniform: skip rounds that hold no k this CTA reads
+      if (!((k0 < khi1 && k0 + 4 * kStride > klo1) || (k0 < khi2 && k0 + 4 * kStride > klo2))) continue;
       uint4 xv[4];
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
@@ -602,11 +615,10 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const int k = k0 + 8 * tid + kStride * v;
-        uint32_t g = gate;
-        const uint2 q = quantise8_fast(xv[v], rc2, g);
-        if (k < K) {
-          *reinterpret_cast<uint2*>(act + m * qs + k) = sc[m] == 0.0f ? make_uint2(0u, 0u) : q;
-          if (!(g >> 31) && sc[m] != 0.0f) redo |= 1u << v;
+        if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {
+          uint32_t g = gate;
+          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(xv[v], rc2, g);
+          redo |= (~g >> 31) << v;
         }
       }
       if (__any_sync(0xffffffffu, redo != 0)) {  // rare
@@ -748,6 +760,33 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
       }
     }
   }
+  // k ranges of the activations this CTA's blocks read: the start item's groups [ga, G) of
+  // its first tile and, for a range that ends in a second tile, [0, gb) of that tile; with
+  // whole tiles in between, everything
+  int klo1 = 0, khi1 = p.K, klo2 = 0, khi2 = 0;
+  {
+    uint32_t t;
+    int ga, gb;
+    order.get(0, t, ga, gb);
+    if (order.n_items == 1) {
+      klo1 = ga * kGroup;
+      khi1 = gb * kGroup;
+    } else if (order.n_items == 2) {
+      int ga1, gb1;
+      order.get(1, t, ga1, gb1);
+      if (gb1 < ga) {
+        klo1 = 0;
+        khi1 = gb1 * kGroup;
+        klo2 = ga * kGroup;
+        khi2 = p.K;
+      }
+    }
+  }
+  if constexpr (FUSED) {
+    // bring the row-scale tables into the constant cache while the previous grid runs
+    const uint32_t warm = kScaleSig[(tid * 4) & 127] ^ kRcpSig[(tid * 4) & 127];
+    asm volatile("" ::"r"(warm));
+  }
   // activations (and y, the workspace) belong to the previous grid until it has completed
   dev::pdl_wait_prior_grids();
   uint4 hdr0 = make_uint4(0, 0, 0, 0), hdr1 = make_uint4(0, 0, 0, 0);
@@ -784,7 +823,8 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
     }
   }
   if constexpr (FUSED) {
-    quantise_prologue<M>(act, p.K, p.act_stride, tid, lane, warp, s_scratch, s_as, p.launch_id);
+    quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
+                         p.launch_id);
   } else {
     if (tid < M) s_as[tid] = ascale_in;
   }
