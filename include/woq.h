@@ -76,7 +76,9 @@ WOQ_API int woq_version(void);
 /* Human-readable name of a status code. Never NULL. */
 WOQ_API const char* woq_status_string(int status);
 
-/* Largest supported M (activation rows). */
+/* Largest supported M (activation rows): 8 for int4 weights and act_quant.  int6
+ * GEMV / linear launches take M <= 4 (WOQ_ERR_SHAPE above).  int4 launches with
+ * M = 5 .. 8 run on the f16 tensor-core consumer (its cost does not grow with M). */
 WOQ_API int woq_max_m(void);
 
 /* Largest supported K for a GEMV (fused = 0) or bf16 linear (fused = 1) launch with
@@ -191,7 +193,8 @@ WOQ_API int woq_w6a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, cons
  *   Same inputs and outputs as woq_w4a8_linear_bf16, without a workspace: its
  *   scratch is a 2 MiB array built into the library, present on every GPU that
  *   loads it until the process exits (enough for M <= 4 with grids of up to 255
- *   CTAs; a shape whose launch would need more returns WOQ_ERR_WORKSPACE).
+ *   CTAs, and for larger M with fewer CTAs; a shape whose launch would need more
+ *   returns WOQ_ERR_WORKSPACE).
  *   The first call on each device looks up the array's device address (with that
  *   device current); make that first call before any stream capture.  Every call
  *   zeroes the part of the scratch it uses (an asynchronous memset on the stream)

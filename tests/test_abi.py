@@ -48,7 +48,7 @@ def test_status_strings(woq):
     for s in range(8):
         assert woq.lib.woq_status_string(s)
     assert woq.lib.woq_status_string(99) == b"unknown status"
-    assert woq.woq_max_m() == 4
+    assert woq.woq_max_m() == 8
     assert woq.woq_version() >= 100
 
 
@@ -98,7 +98,7 @@ def test_linear_and_act_quant_host_validation(woq):
         woq.WOQ_ERR_NULL
     assert L.woq_w4a8_linear_bf16(P(FAKE), 10 ** 9, P(FAKE + 2), 1, 128, 128, P(FAKE), P(FAKE), 10 ** 9, None) == \
         woq.WOQ_ERR_ALIGN
-    assert L.woq_act_quant_int8(P(FAKE), 5, 128, P(FAKE), P(FAKE), None) == woq.WOQ_ERR_SHAPE
+    assert L.woq_act_quant_int8(P(FAKE), 9, 128, P(FAKE), P(FAKE), None) == woq.WOQ_ERR_SHAPE
     assert L.woq_act_quant_int8(P(FAKE), 0, 128, None, None, None) == woq.WOQ_OK
     assert L.woq_act_quant_int8(None, 1, 128, P(FAKE), P(FAKE), None) == woq.WOQ_ERR_NULL
     assert L.woq_act_quant_int8(P(FAKE + 1), 1, 128, P(FAKE), P(FAKE), None) == woq.WOQ_ERR_ALIGN

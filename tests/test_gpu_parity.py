@@ -123,7 +123,7 @@ def run_linear(bits, wdev, x_dev, N, K, M, ws=None):
 
 # --------------------------------------------------------------------------- act_quant
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("K", [128, 1000, 5120, 17408])
 def test_act_quant_bit_exact(M, K):
     x = synthetic.activations(M, K, seed=1000 + M * 7 + K, outliers=True)
@@ -144,8 +144,7 @@ def test_act_quant_bit_exact(M, K):
 
 # --------------------------------------------------------------------------- group dots
 
-@pytest.mark.parametrize("bits", [4, 6])
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("bits,M", [(4, 1), (4, 4), (4, 8), (6, 1), (6, 4)])
 @pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (129, 128)])
 def test_group_dots_bit_exact(bits, M, N, K):
     w, s = make_weights(bits, N, K, seed=N + K + bits)
@@ -205,6 +204,56 @@ def test_fused_linear_matches_oracle_and_separate_path(bits, path, M, N, K, cons
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
+# M = 5 .. 8 (int4 only): the launch table runs the tensor-core consumer
+@pytest.mark.parametrize("M", [5, 6, 7, 8])
+@pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (129, 128), (640, 2048)])
+def test_gemv_wide_m_matches_oracle(M, N, K):
+    bits = 4
+    w, s = make_weights(bits, N, K, seed=13 * N + K + M)
+    wn, sn = to_numpy_u8(w), to_numpy_u16(s)
+    x = synthetic.activations(M, K, seed=N + 5 * M, outliers=True)
+    q_ref, s_ref = oracle.act_quant(to_numpy_u16(x))
+    y_ref, S = oracle.gemv(bits, wn, sn, N, K, q_ref, s_ref)
+    wdev = pack_host(bits, wn, sn, N, K)
+    y = run_gemv(bits, wdev, torch.from_numpy(q_ref).to(DEV), torch.from_numpy(s_ref).to(DEV), N, K, M)
+    ok, worst = tol_ok(y, y_ref, S)
+    assert ok, f"max err / tolerance = {worst}"
+
+
+@pytest.mark.parametrize("M", [5, 8])
+@pytest.mark.parametrize("N,K", [(1000, 1024), (2048, 4096), (300, 5120)])
+def test_fused_linear_wide_m(M, N, K):
+    bits = 4
+    w, s = make_weights(bits, N, K, seed=17 * N + K + M)
+    wn, sn = to_numpy_u8(w), to_numpy_u16(s)
+    xn = to_numpy_u16(synthetic.activations(M, K, seed=7 * N + M, outliers=True))
+    xn[M - 2] = 0  # an all-zero row
+    y_ref, S = oracle.linear_bf16(bits, wn, sn, N, K, xn)
+    wdev = pack_host(bits, wn, sn, N, K)
+    x_dev = torch.from_numpy(xn.view(np.int16)).to(DEV).view(torch.bfloat16)
+    y = run_linear(bits, wdev, x_dev, N, K, M)
+    ok, worst = tol_ok(y, y_ref, S)
+    assert ok, f"max err / tolerance = {worst}"
+    assert not y[M - 2].any()
+    q = torch.empty((M, K), dtype=torch.int8, device=DEV)
+    a = torch.empty((M,), dtype=torch.float32, device=DEV)
+    woq.woq_act_quant_int8(x_dev, q, a)
+    y2 = run_gemv(bits, wdev, q, a, N, K, M)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
+def test_int6_refuses_more_than_four_rows():
+    N, K, M = 128, 256, 5
+    w = torch.empty(woq.woq_packed_bytes(6, N, K), dtype=torch.uint8, device=DEV)
+    x = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((M, N), device=DEV)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device=DEV)
+    with pytest.raises(woq.WoqError) as e:
+        woq.woq_w6a8_linear_bf16(w, x, N, K, y, ws)
+    assert e.value.status == woq.WOQ_ERR_SHAPE
+    assert woq.woq_workspace_bytes(6, M, N, K) == 0 and woq.woq_max_k(6, M, 1) == 0
+
+
 @pytest.mark.parametrize("path", [DP4A, MMA])
 def test_repeated_launches_are_bit_identical(path, consumer):
     consumer(path)
@@ -255,7 +304,7 @@ def test_launch_configurations_agree(cps, stages, pf, path, consumer):
 
 def test_max_k_bounds():
     for bits in (4, 6):
-        for M in (1, 2, 3, 4):
+        for M in range(1, 9 if bits == 4 else 5):
             k8, kb = woq.woq_max_k(bits, M, False), woq.woq_max_k(bits, M, True)
             assert k8 % 128 == 0 and kb % 128 == 0 and 0 < kb <= k8 and M * k8 <= 98304
     # the decode shapes of the 27B and 9B workloads fit the fused entry at M = 4

@@ -54,7 +54,7 @@ def test_noalloc_rejects_oversized_and_bad_arguments():
     import ctypes
     import weight_only_quantised_gb300 as woq
     L = woq.lib
-    assert L.woq_w4a8_linear_bf16_noalloc(None, 0, None, 5, 128, 128, None, None) == woq.WOQ_ERR_SHAPE
+    assert L.woq_w4a8_linear_bf16_noalloc(None, 0, None, 9, 128, 128, None, None) == woq.WOQ_ERR_SHAPE
     assert L.woq_w4a8_linear_bf16_noalloc(None, 0, None, 0, 128, 128, None, None) == woq.WOQ_OK
     y = torch.empty(16, device="cuda:0")
     assert L.woq_w4a8_linear_bf16_noalloc(None, 0, ctypes.c_void_p(0x10000), 1, 128, 128, y.data_ptr(),

@@ -79,17 +79,20 @@ static int ring_offset(int M, int K, bool fused, int cons) {
   return (int)align_up((size_t)act_offset(M, K, fused, cons) + (size_t)act_bytes(M, K, fused, cons), 128);
 }
 
-// Consumer of the int4 kernels (kern::Consumer).  dp4a for every M <= 4: on this part the
-// f16 MMA (mma.sync, fp32 accumulate) costs about what dp4a costs at M = 4 and more below
-// it, and the two contend when mixed in one SM sub-partition.  The MMA's cost does not grow
-// with M; it stays selectable with woq_tune_path.  int6 is always dp4a.
+// Consumer of the int4 kernels (kern::Consumer).  dp4a for M <= 4: on this part the f16
+// MMA (mma.sync, fp32 accumulate) costs about what dp4a costs at M = 4 and more below it,
+// and the two contend when mixed in one SM sub-partition.  The MMA's cost does not grow with
+// M, so it takes M = 5 .. 8 (no dp4a kernel exists there); for M <= 4 woq_tune_path can
+// select it.  int6 is always dp4a (M <= 4).
 int choose_consumer(int bits, int M) {
-  (void)M;
   if (bits != 4) return kern::kDp4a;
+  if (M > kMaxMDp4a) return kern::kMma;
   const int path = g_override_path.load(std::memory_order_relaxed);
   if (path > 0) return path - 1;
   return kern::kDp4a;
 }
+
+static int max_m_for(int bits) { return bits == 4 ? kMaxM : kMaxMDp4a; }
 
 int smem_bytes_for(int bits, int M, int K, bool fused, int stages) {
   return ring_offset(M, K, fused, choose_consumer(bits, M)) + stages * kStageBlocks * block_bytes(bits);
@@ -194,7 +197,7 @@ int woq_tune_path(int path) {
 }
 
 int woq_max_k(int bits, int M, int fused) {
-  if ((bits != 4 && bits != 6) || M < 1 || M > kMaxM) return 0;
+  if ((bits != 4 && bits != 6) || M < 1 || M > max_m_for(bits)) return 0;
   const int smem_max = max_dynamic_smem();
   if (smem_max <= 0) return 0;
   int K = (int)(kMaxMK / M) / kGroup * kGroup;
@@ -203,7 +206,7 @@ int woq_max_k(int bits, int M, int fused) {
 }
 
 size_t woq_workspace_bytes(int bits, int M, int N, int K) {
-  if ((bits != 4 && bits != 6) || M < 0 || M > kMaxM || N < 0 || K < 0 || K % kGroup) return 0;
+  if ((bits != 4 && bits != 6) || M < 0 || M > max_m_for(bits) || N < 0 || K < 0 || K % kGroup) return 0;
   if (M == 0 || N == 0 || K == 0) return 256;  // empty shapes launch nothing
   const int c = max_ctas_for_workspace();
   if (c <= 0) return 0;
@@ -254,7 +257,7 @@ int woq_act_quant_int8(const void* x_bf16, int M, int K, int8_t* q, float* ascal
 static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_bytes, const void* x_bf16,
                     const int8_t* q, const float* ascale, int M, int N, int K, float* y, void* ws, size_t ws_bytes,
                     cudaStream_t stream) {
-  if (M < 0 || M > kMaxM || N < 0 || K < 0 || K % kGroup || (long)M * K > kMaxMK) return WOQ_ERR_SHAPE;
+  if (M < 0 || M > max_m_for(bits) || N < 0 || K < 0 || K % kGroup || (long)M * K > kMaxMK) return WOQ_ERR_SHAPE;
   if (M == 0 || N == 0) return WOQ_OK;  // nothing to compute
   if (!y) return WOQ_ERR_NULL;
   if (!aligned(y, 4)) return WOQ_ERR_ALIGN;

@@ -495,7 +495,7 @@ __device__ __forceinline__ uint32_t absmax8(uint32_t acc, uint4 v) {
 }
 
 // Per-row amax partials of this thread -> every thread's row scales and reciprocals
-// (one barrier).  s_scratch holds [4 rows][8 warps] partials.
+// (one barrier).  s_scratch holds [M rows][8 warps] partials.
 template <int M>
 __device__ __forceinline__ void row_scales(const float (&lmax)[M], int tid, int lane, int warp, float* s_scratch,
                                            float* s_as, float (&sc)[M], float (&rc)[M]) {
@@ -638,6 +638,7 @@ enum Consumer { kDp4a = 0, kMma = 1 };
 template <int BITS, int M, bool FUSED, int CONS>
 __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 288 threads x 112 fit one SM
   static_assert(CONS == kDp4a || BITS == 4, "the tensor-core consumer reads int4 blocks");
+  static_assert(CONS == kMma || M <= kMaxMDp4a, "dp4a kernels take up to four activation rows");
   constexpr int BB = Fmt<BITS>::kBlockBytes;
   constexpr int kStageBytes = kSB * BB;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -646,7 +647,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   uint64_t* actbar = full + 16;                                // activations landed
   volatile int* s_flags = reinterpret_cast<volatile int*>(smem + 136);  // [0] ticket-last, [1] abort, [2] header-ok
   float* s_as = reinterpret_cast<float*>(smem + 160);          // [M] activation scales
-  float* s_scratch = reinterpret_cast<float*>(smem + 192);     // [4 rows][8 warps] amax partials, to byte 320
+  float* s_scratch = reinterpret_cast<float*>(smem + 192);     // [8 rows][8 warps] amax partials, to byte 448
   uint8_t* act = smem + p.act_offset;                          // bf16 x, quantised in place (fused) or int8 q
   float* red = reinterpret_cast<float*>(smem + p.red_offset);  // [4 blocks][M][128 rows]
   uint8_t* ring = smem + p.ring_offset;
@@ -952,7 +953,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
           if (tid == 0) WOQ_TRACE_EV(12 + (item == 0 ? 0 : 2));
           // issue the loads of up to kBatch partner parts at once (one round trip), then poll
           // only the words that were not there yet; sum in CTA order
-          constexpr int kBatch = M == 1 ? 8 : (M == 2 ? 4 : 2);  // bounded by registers
+          constexpr int kBatch = M == 1 ? 8 : (M == 2 ? 4 : (M <= 4 ? 2 : 1));  // bounded by registers
           float tot[M];
 #pragma unroll
           for (int m = 0; m < M; ++m) tot[m] = 0.0f;

@@ -42,8 +42,18 @@ cudaError_t launch_gemv_m(int M, const GemvParams& p, const LaunchConfig& cfg, c
     case 2: return launch_gemv_instance<BITS, 2, FUSED, CONS>(p, cfg, stream);
     case 3: return launch_gemv_instance<BITS, 3, FUSED, CONS>(p, cfg, stream);
     case 4: return launch_gemv_instance<BITS, 4, FUSED, CONS>(p, cfg, stream);
-    default: return cudaErrorInvalidValue;
+    default: break;
   }
+  if constexpr (CONS == kern::kMma) {  // five to eight rows: tensor-core consumer only
+    switch (M) {
+      case 5: return launch_gemv_instance<BITS, 5, FUSED, CONS>(p, cfg, stream);
+      case 6: return launch_gemv_instance<BITS, 6, FUSED, CONS>(p, cfg, stream);
+      case 7: return launch_gemv_instance<BITS, 7, FUSED, CONS>(p, cfg, stream);
+      case 8: return launch_gemv_instance<BITS, 8, FUSED, CONS>(p, cfg, stream);
+      default: break;
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int BITS, int CONS>

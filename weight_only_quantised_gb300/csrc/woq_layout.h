@@ -65,7 +65,8 @@ constexpr int kW4Bytes = kTileRows * kGroup / 2;           // 8192
 constexpr int kHiBytes = kTileRows * kGroup / 4;           // 4096 (2 bits per weight)
 constexpr int kBlockBytesW4 = kScaleBytes + kW4Bytes;      // 8448
 constexpr int kBlockBytesW6 = kScaleBytes + kW4Bytes + kHiBytes;  // 12544
-constexpr int kMaxM = 4;
+constexpr int kMaxM = 8;      // activation rows (int4); int6 and the dp4a kernels take up to kMaxMDp4a
+constexpr int kMaxMDp4a = 4;
 constexpr long kMaxMK = 98304;  // shared-memory bound on M * K for the activation tile
 
 // Header (little-endian, 256 bytes; unused bytes zero).

@@ -228,6 +228,10 @@ static cudaError_t launch_dots_bits(const void* wpacked, const int8_t* q, int M,
     case 2: kern::group_dots_kernel<BITS, 2><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
     case 3: kern::group_dots_kernel<BITS, 3><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
     case 4: kern::group_dots_kernel<BITS, 4><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
+    case 5: kern::group_dots_kernel<BITS, 5><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
+    case 6: kern::group_dots_kernel<BITS, 6><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
+    case 7: kern::group_dots_kernel<BITS, 7><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
+    case 8: kern::group_dots_kernel<BITS, 8><<<blocks, threads, 0, stream>>>(w, q, N, K, dots); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
