@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--linear", default="", help="time one 27B-class linear (qkv, o, gate_up, down, lm_head) "
                                                  "instead of the step: a graph of launches over distinct weight copies")
     ap.add_argument("--int8", action="store_true", help="with --linear: the int8 entry (act_quant once, then GEMV)")
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
+                    help="with --linear: int4 consumer (0 launch table, 1 dp4a, 2 tensor-core MMA)")
     return ap.parse_args()
 
 
@@ -357,7 +359,7 @@ def run_ours(args):
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_kind": peak_kind, "kernel": "woq::kern::gemv_kernel<4, M, fused>",
+                     "peak_kind": peak_kind, "kernel": "woq::kern::gemv_kernel<4, M, fused, dp4a>",
                      "per": "step (257 launches)"},
         "extra_m": extra,
         "e2e": e2e,
@@ -447,6 +449,7 @@ def run_linear(args):
     M = args.m
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    woq.woq_tune_path(args.path)
     pb = woq.woq_packed_bytes(4, N, K)
     copies = max(4, int(1.2e9 // pb))
     w, s = synthetic.weights(4, N, K, synthetic.sub_seed(2, args.linear), device=dev)
@@ -489,6 +492,7 @@ def run_linear(args):
     nbytes = N * K // 2 + 2 * N * (K // 128) + (M * K if args.int8 else 2 * M * K)
     peak, kind = measured_peak()
     print(json.dumps({"linear": args.linear, "K": K, "N": N, "m": M, "entry": "int8" if args.int8 else "bf16",
+                      "consumer": {0: "table", 1: "dp4a", 2: "mma"}[args.path],
                       "us_per_launch": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
                       "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "peak_kind": kind,
                       "launches_per_graph": copies}), flush=True)
