@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--linear", default="", help="time one 27B-class linear (qkv, o, gate_up, down, lm_head) "
                                                  "instead of the step: a graph of launches over distinct weight copies")
     ap.add_argument("--int8", action="store_true", help="with --linear: the int8 entry (act_quant once, then GEMV)")
+    ap.add_argument("--tree-planner", action="store_true",
+                    help="time one re-plan of the draft-tree planner (host code) against its oracle")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
                     help="with --linear: int4 consumer (0 launch table, 1 dp4a, 2 tensor-core MMA)")
     return ap.parse_args()
@@ -498,8 +500,43 @@ def run_linear(args):
                       "launches_per_graph": copies}), flush=True)
 
 
+def run_tree_planner(args):
+    """Draft-tree planner re-plan time: all 64 shapes scored (library), and the oracle's."""
+    import random
+
+    import weight_only_quantised_gb300 as woq
+    from oracle import tree as T
+    rng = random.Random(3)
+    lib, ora = woq.TreePlanner(replan_every=10 ** 9), T.Planner(replan_every=10 ** 9)
+    probs = []
+    for _ in range(7):
+        w = [rng.random() for _ in range(8)]
+        probs.append([x / sum(w) for x in w])
+    for _ in range(256):  # synthetic acceptance statistics
+        _, ranks = T.simulate_step(probs, ora.shape, rng)
+        lib.observe(ranks, 0.08, 1.0)
+        ora.observe(ranks, 0.08, 1.0)
+    n = max(1000, args.steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        lib.replan()
+    lib_us = (time.perf_counter() - t0) / n * 1e6
+    m = 200
+    t0 = time.perf_counter()
+    for _ in range(m):
+        ora.replan()
+    ora_us = (time.perf_counter() - t0) / m * 1e6
+    print(json.dumps({"metric": "draft-tree planner re-plan time (64 shapes)", "value": round(lib_us, 3), "unit": "us",
+                      "higher_is_better": False, "calls": n, "note": "host code, called through ctypes",
+                      "cpu_baseline": {"value": round(ora_us, 2), "unit": "us", "cores": 1, "kind": "oracle",
+                                       "sample": f"{m} re-plans"}}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.tree_planner:
+        run_tree_planner(args)
+        return
     if args.linear:
         run_linear(args)
         return

@@ -1,5 +1,5 @@
 """The C ABI library builds, loads without a GPU, exports every symbol that
-include/woq.h declares, and rejects invalid arguments on the host (these
+include/*.h declares, and rejects invalid arguments on the host (these
 checks run before any CUDA call, so no GPU is needed)."""
 import ctypes
 import os
@@ -21,9 +21,13 @@ def woq():
 
 
 def declared_functions():
-    with open(os.path.join(ROOT, "include", "woq.h")) as f:
-        text = f.read()
-    return sorted(set(re.findall(r"^WOQ_API\s+[\w\s\*]+?\b(woq_\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        if h.endswith(".h"):
+            with open(os.path.join(inc, h)) as f:
+                names |= set(re.findall(r"^WOQ_API\s+[\w\s\*]+?\b(woq_\w+)\s*\(", f.read(), flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():

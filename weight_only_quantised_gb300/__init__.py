@@ -229,3 +229,74 @@ def woq_tune_override(ctas_per_sm: int = 0, stages: int = 0, prefetch_kb: int = 
 def woq_tune_path(path: int = 0) -> None:
     """int4 consumer of later launches: 0 launch table, 1 dp4a, 2 tensor-core MMA."""
     _check(lib.woq_tune_path(path), "woq_tune_path")
+
+
+# ----------------------------------------------------------------------------- draft-tree planner
+# (include/woq_tree.h; host code in the same library)
+
+_TREE_ROWS, _TREE_BINS, TREE_SHAPES = 7, 8, 64
+
+
+class TreePlannerState(ctypes.Structure):
+    _fields_ = [("counts", (ctypes.c_double * _TREE_BINS) * _TREE_ROWS),
+                ("draft_ms", ctypes.c_double), ("verify_ms", ctypes.c_double),
+                ("decay", ctypes.c_double), ("hysteresis", ctypes.c_double),
+                ("replan_every", ctypes.c_int), ("steps", ctypes.c_int), ("times_seen", ctypes.c_int),
+                ("widths", ctypes.c_int * _TREE_ROWS), ("depth", ctypes.c_int)]
+
+
+_TP = ctypes.POINTER(TreePlannerState)
+_IP = ctypes.POINTER(ctypes.c_int)
+_DP = ctypes.POINTER(ctypes.c_double)
+for _name, (_args, _res) in {
+    "woq_tree_init": ([_TP, ctypes.c_double, ctypes.c_double, _I], _I),
+    "woq_tree_shape": ([_I, _IP, _IP], _I),
+    "woq_tree_score": ([_TP, _IP, _I, _DP, _DP], _I),
+    "woq_tree_observe": ([_TP, _I, _IP, ctypes.c_double, ctypes.c_double, _IP], _I),
+    "woq_tree_replan": ([_TP, _IP, _DP, _IP], _I),
+}.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+
+def woq_tree_shape(index: int) -> tuple:
+    w = (ctypes.c_int * _TREE_ROWS)()
+    d = ctypes.c_int()
+    _check(lib.woq_tree_shape(index, w, ctypes.byref(d)), "woq_tree_shape")
+    return tuple(w[: d.value])
+
+
+class TreePlanner:
+    """The draft-tree planner of include/woq_tree.h (argument marshalling only)."""
+
+    def __init__(self, decay: float = 0.0, hysteresis: float = -1.0, replan_every: int = 0):
+        self.state = TreePlannerState()
+        _check(lib.woq_tree_init(ctypes.byref(self.state), decay, hysteresis, replan_every), "woq_tree_init")
+
+    @property
+    def shape(self) -> tuple:
+        return tuple(self.state.widths[: self.state.depth])
+
+    def score(self, widths) -> tuple:
+        w = (ctypes.c_int * _TREE_ROWS)(*widths)
+        e, s = ctypes.c_double(), ctypes.c_double()
+        _check(lib.woq_tree_score(ctypes.byref(self.state), w, len(widths), ctypes.byref(e), ctypes.byref(s)),
+               "woq_tree_score")
+        return e.value, s.value
+
+    def observe(self, ranks, draft_ms: float = -1.0, verify_ms: float = -1.0) -> bool:
+        r = (ctypes.c_int * _TREE_ROWS)(*ranks)
+        sw = ctypes.c_int()
+        _check(lib.woq_tree_observe(ctypes.byref(self.state), len(ranks), r, draft_ms, verify_ms, ctypes.byref(sw)),
+               "woq_tree_observe")
+        return bool(sw.value)
+
+    def replan(self) -> tuple:
+        i, s, sw = ctypes.c_int(), ctypes.c_double(), ctypes.c_int()
+        _check(lib.woq_tree_replan(ctypes.byref(self.state), ctypes.byref(i), ctypes.byref(s), ctypes.byref(sw)),
+               "woq_tree_replan")
+        return i.value, s.value, bool(sw.value)
+
+    def counts(self) -> np.ndarray:
+        return np.array([[self.state.counts[d][b] for b in range(_TREE_BINS)] for d in range(_TREE_ROWS)])

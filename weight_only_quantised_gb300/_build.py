@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwoq.so")
 SOURCES = ["woq_api.cu", "woq_gemv_w4.cu", "woq_gemv_w4_mma.cu", "woq_gemv_w6.cu", "woq_small_kernels.cu",
-           "woq_pack.cpp"]
+           "woq_pack.cpp", "woq_tree.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,7 +30,8 @@ def nvcc() -> str:
 
 
 def _deps_mtime() -> float:
-    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "woq.h"), __file__]
+    inc = os.path.join(ROOT, "include")
+    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(inc, f) for f in os.listdir(inc)] + [__file__]
     return max(os.path.getmtime(p) for p in paths)
 
 
