@@ -76,6 +76,14 @@ def _load():
             lib.oracle_gemv.restype = I
             lib.oracle_linear_bf16.argtypes = [I, P, P, I, I, P, I, P, P]
             lib.oracle_linear_bf16.restype = I
+            lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_exp_cw.argtypes = [ctypes.c_float]
+            lib.oracle_exp_cw.restype = ctypes.c_float
+            lib.oracle_rmsnorm_bf16.argtypes = [P, P, ctypes.c_float, I, I, P]
+            lib.oracle_rmsnorm_bf16.restype = I
+            lib.oracle_swiglu_bf16.argtypes = [P, I, I, P]
+            lib.oracle_swiglu_bf16.restype = I
             _lib = lib
     return _lib
 
@@ -162,3 +170,44 @@ def linear_bf16(bits: int, w: np.ndarray, wscale_f16: np.ndarray, N: int, K: int
 def tolerance(S: np.ndarray) -> np.ndarray:
     """Allowed |y_gpu - y_ref| per element: 1e-5 * sum_g |term_g| + 1e-6."""
     return 1e-5 * np.asarray(S, dtype=np.float64) + 1e-6
+
+
+# ----------------------------------------------------------------------------- prologue fusions (R11 - R13)
+
+def f32_to_bf16(v: float) -> int:
+    """fp32 -> bf16 bit pattern, round to nearest even."""
+    return int(_load().oracle_f32_to_bf16(float(v)))
+
+
+def exp_cw(a: float) -> float:
+    """e^a in fp32 by the Cody-Waite method with a degree-7 Taylor polynomial (R12)."""
+    return float(_load().oracle_exp_cw(float(a)))
+
+
+def rmsnorm(x_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm (R11) of bf16 rows [M, K] with bf16 weights [K] -> bf16 bit patterns [M, K]."""
+    x = _c(x_bf16, np.uint16)
+    g = _c(gamma_bf16, np.uint16)
+    M, K = x.shape
+    h = np.zeros((M, K), dtype=np.uint16)
+    _check(_load().oracle_rmsnorm_bf16(_ptr(x), _ptr(g), float(eps), M, K, _ptr(h)), "rmsnorm")
+    return h
+
+
+def swiglu(gate_up_f32: np.ndarray) -> np.ndarray:
+    """SwiGLU (R12) of fp32 rows [M, 2K] (gate, then up) -> bf16 bit patterns [M, K]."""
+    gu = _c(gate_up_f32, np.float32)
+    M, K2 = gu.shape
+    h = np.zeros((M, K2 // 2), dtype=np.uint16)
+    _check(_load().oracle_swiglu_bf16(_ptr(gu), M, K2 // 2, _ptr(h)), "swiglu")
+    return h
+
+
+def linear_rmsnorm(bits, w, wscale_f16, N, K, x_bf16, gamma_bf16, eps):
+    """RMSNorm, act_quant and the linear (R11, R13, R5, R6): y fp32 [M, N], S fp64 [M, N]."""
+    return linear_bf16(bits, w, wscale_f16, N, K, rmsnorm(x_bf16, gamma_bf16, eps))
+
+
+def linear_swiglu(bits, w, wscale_f16, N, K, gate_up_f32):
+    """SwiGLU, act_quant and the linear (R12, R13, R5, R6): y fp32 [M, N], S fp64 [M, N]."""
+    return linear_bf16(bits, w, wscale_f16, N, K, swiglu(gate_up_f32))

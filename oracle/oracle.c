@@ -37,6 +37,22 @@
  *       and rounded once to fp32;
  *   R7  non-finite activations are outside the domain (rejected here);
  *       subnormals are kept (no flush to zero).
+ *   R11 (prologue fusion, RMSNorm) h = bf16(RN(RN(x * r) * gamma)) per element,
+ *       r = RN(1 / RN(sqrt(RN(RN(ms) + eps)))), where the mean of squares ms is
+ *       formed from exact squares: a bf16 x is a 2^c with a an integer < 256, so
+ *       x^2 = a^2 2^(2c); the row sum S = sum_k floor(a_k^2 2^(2 c_k - 2 C + 30))
+ *       2^(2C - 30) (C the largest c of a nonzero x of the row; an unsigned 64-bit
+ *       integer sum, independent of the order of summation), ms = RN(RN(S) / K).
+ *       An all-zero row gives h = 0.  Rows whose largest |x| is below 2^-40 are
+ *       outside the domain;
+ *   R12 (prologue fusion, SwiGLU) input: the fp32 [M][2K] output of a gate+up
+ *       linear (gate = columns 0 .. K-1, up = K .. 2K-1); h = bf16(RN(RN(g * sg)
+ *       * u)), sg = RN(1 / RN(1 + e)), e = exp(-g) evaluated in fp32 by the
+ *       Cody-Waite method: n = rint(RN(a log2 e)), r = a - n ln2 with ln2 split in
+ *       two constants (two fused multiply-adds), the degree-7 Taylor polynomial of
+ *       e^r by Horner's rule with fused multiply-adds, scaled by 2^n; a >= 88.72
+ *       gives +inf and a <= -87 gives 0;
+ *   R13 both fusions quantise the bf16 h exactly as R5 quantises x.
  *
  * The fp16 and bf16 decoders are written from the IEEE 754 encodings.
  * Build: plain C11, no -ffast-math, -ffp-contract=off.
@@ -44,6 +60,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 
 /* status codes of the oracle's own entry points */
 #define ORACLE_OK 0
@@ -220,4 +237,103 @@ int oracle_linear_bf16(int bits, const uint8_t* w, const uint16_t* wscale_f16, i
   free(q);
   free(as);
   return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* prologue fusions (R11 - R13; section "Optimizing the Linear Kernel": the  */
+/* activation quantisation absorbs the RMSNorm or SwiGLU that precedes it)   */
+/* ------------------------------------------------------------------------ */
+
+/* fp32 -> bf16 bit pattern, round to nearest, ties to even (finite inputs) */
+uint16_t oracle_f32_to_bf16(float v) {
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  const uint32_t keep = u >> 16, rem = u & 0xFFFFu;
+  uint32_t r = keep;
+  if (rem > 0x8000u || (rem == 0x8000u && (keep & 1u))) r = keep + 1u;
+  return (uint16_t)r;
+}
+
+/* e^a in fp32 by Cody-Waite argument reduction and a degree-7 Taylor polynomial */
+float oracle_exp_cw(float a) {
+  if (a >= 88.72f) return INFINITY;
+  if (a <= -87.0f) return 0.0f;
+  const float n = rintf(a * 1.44269504f);
+  float r = fmaf(-n, 0.693359375f, a);
+  r = fmaf(-n, -2.12194440e-4f, r);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, r, 1.0f / 720.0f);
+  p = fmaf(p, r, 1.0f / 120.0f);
+  p = fmaf(p, r, 1.0f / 24.0f);
+  p = fmaf(p, r, 1.0f / 6.0f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  return ldexpf(p, (int)n);
+}
+
+/* a bf16 value as a 2^c with 0 <= a < 256: returns a, writes c */
+static uint32_t bf16_int_exp(uint16_t b, int* c) {
+  const uint32_t ef = (b >> 7) & 0xFFu, f = b & 0x7Fu;
+  if (ef == 0) {
+    *c = -133;
+    return f;
+  }
+  *c = (int)ef - 134;
+  return 128u + f;
+}
+
+int oracle_rmsnorm_bf16(const uint16_t* x, const uint16_t* gamma, float eps, int M, int K, uint16_t* h) {
+  if (M < 0 || K < 0) return ORACLE_ERR_SHAPE;
+  for (int m = 0; m < M; ++m) {
+    const uint16_t* xr = x + (size_t)m * K;
+    uint16_t* hr = h + (size_t)m * K;
+    int C = -1000;
+    for (int k = 0; k < K; ++k) {
+      if (!isfinite(oracle_bf16_to_f32(xr[k]))) return ORACLE_ERR_NONFINITE;
+      int c;
+      if (bf16_int_exp(xr[k], &c) != 0 && c > C) C = c;
+    }
+    if (C == -1000) { /* all zero */
+      for (int k = 0; k < K; ++k) hr[k] = 0;
+      continue;
+    }
+    if (C < -47) return ORACLE_ERR_RANGE; /* largest |x| below 2^-40 */
+    uint64_t S = 0;
+    for (int k = 0; k < K; ++k) {
+      int c;
+      const uint64_t a = bf16_int_exp(xr[k], &c);
+      const int sh = 2 * c - 2 * C + 30; /* a^2 2^(2c) in units of 2^(2C - 30) */
+      if (a == 0) continue;
+      if (sh >= 0)
+        S += (a * a) << sh;
+      else if (sh > -64)
+        S += (a * a) >> (-sh);
+    }
+    const float s1 = (float)S; /* round to nearest */
+    const float ms = ldexpf(s1, 2 * C - 30) / (float)K;
+    const float sd = sqrtf(ms + eps);
+    const float r = 1.0f / sd;
+    for (int k = 0; k < K; ++k) {
+      const float xr_k = oracle_bf16_to_f32(xr[k]) * r;
+      hr[k] = oracle_f32_to_bf16(xr_k * oracle_bf16_to_f32(gamma[k]));
+    }
+  }
+  return ORACLE_OK;
+}
+
+int oracle_swiglu_bf16(const float* gu, int M, int K, uint16_t* h) {
+  if (M < 0 || K < 0) return ORACLE_ERR_SHAPE;
+  for (int m = 0; m < M; ++m) {
+    const float* g = gu + (size_t)m * 2 * K;
+    const float* u = g + K;
+    for (int k = 0; k < K; ++k) {
+      if (!isfinite(g[k]) || !isfinite(u[k])) return ORACLE_ERR_NONFINITE;
+      const float e = oracle_exp_cw(-g[k]);
+      const float sg = 1.0f / (1.0f + e);
+      const float si = g[k] * sg;
+      h[(size_t)m * K + k] = oracle_f32_to_bf16(si * u[k]);
+    }
+  }
+  return ORACLE_OK;
 }

@@ -280,3 +280,97 @@ def test_empty_shapes():
     y, S = oracle.gemv(4, np.zeros((3, 0), np.uint8), np.zeros((3, 0), np.uint16), 3, 0,
                        np.zeros((1, 0), np.int8), np.ones(1, np.float32))
     assert y.shape == (1, 3) and not y.any()
+
+
+# --------------------------------------------------------------------------- prologue fusions (R11 - R13)
+
+def _bf16_bits(t):
+    import torch
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_value(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_f32_to_bf16_is_round_to_nearest_even():
+    import torch
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    # exact ties: low 16 bits 0x8000 with even and odd kept parts
+    ties = (np.arange(2000, dtype=np.uint32) * 0x10000 + 0x3F808000).view(np.float32)
+    for x in np.concatenate([v, ties]):
+        assert oracle.f32_to_bf16(float(x)) == int(_bf16_bits(torch.tensor([x]))[0])
+
+
+def test_exp_cw_within_two_ulp_of_exp():
+    import math
+    xs = np.concatenate([np.linspace(-86.9, 88.6, 40001, dtype=np.float32),
+                         np.float32([0.0, 1e-8, -1e-8, 0.5, -0.5, 0.6931472, -0.6931472])])
+    worst = 0.0
+    for x in xs:
+        e = oracle.exp_cw(float(x))
+        ref = math.exp(float(x))
+        ulp = float(np.spacing(np.float32(ref)))  # fp32 spacing at the result
+        worst = max(worst, abs(e - ref) / ulp)
+    assert worst <= 2.0, worst
+    assert oracle.exp_cw(0.0) == 1.0
+    assert oracle.exp_cw(88.72) == float("inf") and oracle.exp_cw(-87.0) == 0.0
+
+
+def test_swiglu_matches_fp64_within_one_bf16_step():
+    rng = np.random.default_rng(5)
+    M, K = 3, 2048
+    gu = (rng.standard_normal((M, 2 * K)) * 3).astype(np.float32)
+    gu[0, :8] = [0.0, -0.0, 50.0, -50.0, 100.0, -100.0, 1e-30, -1e-30]
+    h = oracle.swiglu(gu)
+    g = gu[:, :K].astype(np.float64)
+    u = gu[:, K:].astype(np.float64)
+    ref = g / (1.0 + np.exp(-g)) * u
+    hv = _bf16_value(h)
+    step = np.maximum(np.abs(ref), 1e-38) * 2.0 ** -7  # one bf16 step at the value
+    assert (np.abs(hv - ref) <= step).all()
+    assert hv[0, 0] == 0 and hv[0, 5] == 0  # silu(0) = 0, silu(-100) = -0
+    assert abs(hv[0, 4] - 100.0 * u[0, 4]) <= abs(100.0 * u[0, 4]) * 2.0 ** -8
+
+
+def test_rmsnorm_matches_fp64_and_its_invariants():
+    import torch
+    rng = np.random.default_rng(6)
+    M, K = 4, 5120
+    x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32))
+    x[:, ::97] *= 20.0
+    xb = _bf16_bits(x)
+    gamma = _bf16_bits(torch.from_numpy((1.0 + 0.1 * rng.standard_normal(K)).astype(np.float32)))
+    eps = 1e-6
+    h = oracle.rmsnorm(xb, gamma, eps)
+    xv, gv = _bf16_value(xb), _bf16_value(gamma)
+    ref = xv / np.sqrt((xv ** 2).mean(axis=1, keepdims=True) + eps) * gv
+    assert (np.abs(_bf16_value(h) - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30).all()
+    # scaling x by a power of two leaves h unchanged (eps = 0): the squares are exact
+    h0 = oracle.rmsnorm(xb, gamma, 0.0)
+    for j in (-9, 3, 11):
+        xs = _bf16_bits(torch.from_numpy((xv * 2.0 ** j).astype(np.float32)))
+        assert np.array_equal(oracle.rmsnorm(xs, gamma, 0.0), h0)
+    # all-zero row gives zeros; a constant row with gamma = 1 gives +-1
+    z = np.zeros((1, 256), np.uint16)
+    assert not oracle.rmsnorm(z, np.full(256, 0x3F80, np.uint16), 1e-6).any()
+    c = np.full((1, 256), 0xC040, np.uint16)  # -3.0
+    assert (oracle.rmsnorm(c, np.full(256, 0x3F80, np.uint16), 0.0) == 0xBF80).all()  # -1.0
+
+
+def test_fused_linear_oracles_compose_the_steps():
+    rng = np.random.default_rng(7)
+    N, K, M = 64, 256, 2
+    wv = rng.integers(-8, 8, size=(N, K))
+    w = encode_w4(wv)
+    s = (np.abs(rng.standard_normal((N, K // 128))) * 0.02 + 1e-3).astype(np.float16).view(np.uint16)
+    gu = rng.standard_normal((M, 2 * K)).astype(np.float32)
+    y, S = oracle.linear_swiglu(4, w, s, N, K, gu)
+    y2, _ = oracle.linear_bf16(4, w, s, N, K, oracle.swiglu(gu))
+    assert np.array_equal(y, y2)
+    x = rng.integers(0, 1 << 16, size=(M, K), dtype=np.uint16) & 0xBFFF  # finite values
+    g = np.full(K, 0x3F80, np.uint16)
+    y3, _ = oracle.linear_rmsnorm(4, w, s, N, K, x, g, 1e-5)
+    y4, _ = oracle.linear_bf16(4, w, s, N, K, oracle.rmsnorm(x, g, 1e-5))
+    assert np.array_equal(y3, y4)
