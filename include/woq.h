@@ -186,6 +186,46 @@ WOQ_API int woq_w6a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, cons
                          void* ws, size_t ws_bytes, woq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Prologue fusions (section "Optimizing the Linear Kernel": the activation
+ * quantisation absorbs the RMSNorm or SwiGLU that precedes the linear, so the
+ * intermediate tensor is never written to memory).  One launch each; h is
+ * formed in shared memory, rounded to bf16, then quantised exactly as
+ * woq_act_quant_int8 quantises x.
+ *
+ * RMSNorm: x_bf16 device bf16 [M][K], gamma_bf16 device bf16 [K] (16-byte
+ *   aligned), eps >= 0.  h = bf16(RN(RN(x r) gamma)), r = RN(1 / RN(sqrt(RN(ms +
+ *   eps)))), the mean of squares ms formed from the exact squares of the bf16 x,
+ *   summed as integers at a per-row fixed point (order independent) and rounded
+ *   once: ms = RN(RN(S) / K).  An all-zero row (or one whose largest |x| is below
+ *   2^-40) gives h = 0.
+ * SwiGLU: gate_up device fp32 [M][2K] (the output of a gate+up linear: gate in
+ *   columns 0 .. K-1, up in K .. 2K-1), 16-byte aligned.  h = bf16(RN(RN(g sg) u)),
+ *   sg = RN(1 / RN(1 + e)), e = e^-g in fp32 by Cody and Waite's reduction and a
+ *   degree-7 Taylor polynomial (fused multiply-adds), scaled by 2^n.
+ * Otherwise as woq_w4a8_linear_bf16 (the same bounds on M, N, K; K <=
+ * woq_max_k(bits, M, 1)).  Each is bit-identical to its woq_*_act_quant_int8
+ * twin below followed by woq_w4a8_gemv / woq_w6a8_gemv.
+ * --------------------------------------------------------------------------- */
+WOQ_API int woq_w4a8_linear_rmsnorm_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16,
+                                         const void* gamma_bf16, float eps, int M, int N, int K, float* y, void* ws,
+                                         size_t ws_bytes, woq_stream_t stream);
+WOQ_API int woq_w6a8_linear_rmsnorm_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16,
+                                         const void* gamma_bf16, float eps, int M, int N, int K, float* y, void* ws,
+                                         size_t ws_bytes, woq_stream_t stream);
+WOQ_API int woq_w4a8_linear_swiglu_f32(const void* wpacked, size_t wpacked_bytes, const float* gate_up, int M, int N,
+                                       int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream);
+WOQ_API int woq_w6a8_linear_swiglu_f32(const void* wpacked, size_t wpacked_bytes, const float* gate_up, int M, int N,
+                                       int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream);
+
+/* Unfused twins: RMSNorm (or SwiGLU) then act_quant, writing q int8 [M][K] and
+ * ascale fp32 [M] like woq_act_quant_int8.  K % 8 == 0, 2 K bytes of shared memory
+ * per row (K <= 113,664); otherwise as the fused forms. */
+WOQ_API int woq_rmsnorm_act_quant_int8(const void* x_bf16, const void* gamma_bf16, float eps, int M, int K, int8_t* q,
+                                       float* ascale, woq_stream_t stream);
+WOQ_API int woq_swiglu_act_quant_int8(const float* gate_up, int M, int K, int8_t* q, float* ascale,
+                                      woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Allocation-free variant of woq_w4a8_linear_bf16 (the pages have no counterpart:
  * this is a service for callers that cannot allocate device memory, such as
  * plugins inside a host application that owns every device allocation, or loops

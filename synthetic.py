@@ -14,7 +14,9 @@ Recipe (the workloads of the decode linears of 9B- and 27B-class decoders):
     c, eps = 0.02, 1e-3 for int4 and 0.005, 1e-4 for int6;
   * activations: N(0,1) in fp32; optionally round(0.01 * K) outlier channels,
     picked once per matrix by a seeded permutation and shared by all rows,
-    are multiplied by 20; then rounded once to bf16.
+    are multiplied by 20; then rounded once to bf16;
+  * RMSNorm weights: 1 + 0.1 N(0,1) in fp32, rounded to bf16;
+  * gate+up outputs (the SwiGLU prologue's input): 2 N(0,1) in fp32.
 
 All draws use torch generators, so the same call gives the same bits for a
 given device type; tests generate once and hand the same arrays to both sides.
@@ -74,6 +76,20 @@ def activations(M: int, K: int, seed: int, outliers: bool = True, device="cpu") 
         idx = torch.randperm(K, generator=gp)[:n_out].to(dev)
         x[:, idx] *= 20.0
     return x.to(torch.bfloat16)
+
+
+def rmsnorm_weight(K: int, seed: int, device="cpu") -> torch.Tensor:
+    """bf16 RMSNorm weights [K]: 1 + 0.1 N(0,1)."""
+    dev = torch.device(device)
+    g = _gen(sub_seed(seed, "gamma", K), dev)
+    return (1.0 + 0.1 * torch.randn((K,), dtype=torch.float32, generator=g, device=dev)).to(torch.bfloat16)
+
+
+def gate_up_output(M: int, K: int, seed: int, device="cpu") -> torch.Tensor:
+    """fp32 [M, 2K] stand-in for a gate+up linear's output (gate, then up): N(0,1) * 2."""
+    dev = torch.device(device)
+    g = _gen(sub_seed(seed, "gate_up", M, K), dev)
+    return 2.0 * torch.randn((M, 2 * K), dtype=torch.float32, generator=g, device=dev)
 
 
 def to_numpy_u16(t: torch.Tensor) -> np.ndarray:

@@ -62,6 +62,12 @@ _SIGS = {
     "woq_w4a8_linear_bf16_noalloc": ([_P, _Z, _P, _I, _I, _I, _P, _P], _I),
     "woq_tune_override": ([_I, _I, _I], _I),
     "woq_tune_path": ([_I], _I),
+    "woq_w4a8_linear_rmsnorm_bf16": ([_P, _Z, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "woq_w6a8_linear_rmsnorm_bf16": ([_P, _Z, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "woq_w4a8_linear_swiglu_f32": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "woq_w6a8_linear_swiglu_f32": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
+    "woq_rmsnorm_act_quant_int8": ([_P, _P, ctypes.c_float, _I, _I, _P, _P, _P], _I),
+    "woq_swiglu_act_quant_int8": ([_P, _I, _I, _P, _P, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -206,6 +212,50 @@ def woq_w4a8_linear_bf16(wpacked, x_bf16, N: int, K: int, y, ws, stream=None) ->
 
 def woq_w6a8_linear_bf16(wpacked, x_bf16, N: int, K: int, y, ws, stream=None) -> None:
     _linear(lib.woq_w6a8_linear_bf16, "woq_w6a8_linear_bf16", wpacked, x_bf16, N, K, y, ws, stream)
+
+
+def _linear_rmsnorm(fn, name, wpacked, x_bf16, gamma_bf16, eps, N, K, y, ws, stream):
+    M = x_bf16.shape[0]
+    _check(fn(_dptr(wpacked), _nbytes(wpacked), _dptr(x_bf16), _dptr(gamma_bf16), float(eps), M, N, K, _dptr(y),
+              _dptr(ws), _nbytes(ws), _stream(stream)), name)
+
+
+def woq_w4a8_linear_rmsnorm_bf16(wpacked, x_bf16, gamma_bf16, eps: float, N: int, K: int, y, ws, stream=None) -> None:
+    """RMSNorm(x) with gamma, quantised and run through the int4 linear, in one launch."""
+    _linear_rmsnorm(lib.woq_w4a8_linear_rmsnorm_bf16, "woq_w4a8_linear_rmsnorm_bf16", wpacked, x_bf16, gamma_bf16, eps,
+                    N, K, y, ws, stream)
+
+
+def woq_w6a8_linear_rmsnorm_bf16(wpacked, x_bf16, gamma_bf16, eps: float, N: int, K: int, y, ws, stream=None) -> None:
+    _linear_rmsnorm(lib.woq_w6a8_linear_rmsnorm_bf16, "woq_w6a8_linear_rmsnorm_bf16", wpacked, x_bf16, gamma_bf16, eps,
+                    N, K, y, ws, stream)
+
+
+def _linear_swiglu(fn, name, wpacked, gate_up, N, K, y, ws, stream):
+    M = gate_up.shape[0]
+    _check(fn(_dptr(wpacked), _nbytes(wpacked), _dptr(gate_up), M, N, K, _dptr(y), _dptr(ws), _nbytes(ws),
+              _stream(stream)), name)
+
+
+def woq_w4a8_linear_swiglu_f32(wpacked, gate_up, N: int, K: int, y, ws, stream=None) -> None:
+    """SwiGLU of an fp32 gate+up output [M, 2K], quantised and run through the int4 linear, in one launch."""
+    _linear_swiglu(lib.woq_w4a8_linear_swiglu_f32, "woq_w4a8_linear_swiglu_f32", wpacked, gate_up, N, K, y, ws, stream)
+
+
+def woq_w6a8_linear_swiglu_f32(wpacked, gate_up, N: int, K: int, y, ws, stream=None) -> None:
+    _linear_swiglu(lib.woq_w6a8_linear_swiglu_f32, "woq_w6a8_linear_swiglu_f32", wpacked, gate_up, N, K, y, ws, stream)
+
+
+def woq_rmsnorm_act_quant_int8(x_bf16, gamma_bf16, eps: float, q, ascale, stream=None) -> None:
+    M, K = x_bf16.shape
+    _check(lib.woq_rmsnorm_act_quant_int8(_dptr(x_bf16), _dptr(gamma_bf16), float(eps), M, K, _dptr(q), _dptr(ascale),
+                                          _stream(stream)), "woq_rmsnorm_act_quant_int8")
+
+
+def woq_swiglu_act_quant_int8(gate_up, q, ascale, stream=None) -> None:
+    M, K2 = gate_up.shape
+    _check(lib.woq_swiglu_act_quant_int8(_dptr(gate_up), M, K2 // 2, _dptr(q), _dptr(ascale), _stream(stream)),
+           "woq_swiglu_act_quant_int8")
 
 
 def woq_w4a8_linear_bf16_noalloc(wpacked, x_bf16, N: int, K: int, y, stream=None) -> None:

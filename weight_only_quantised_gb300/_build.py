@@ -17,8 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwoq.so")
-SOURCES = ["woq_api.cu", "woq_gemv_w4.cu", "woq_gemv_w4_mma.cu", "woq_gemv_w6.cu", "woq_small_kernels.cu",
-           "woq_pack.cpp", "woq_tree.cpp"]
+SOURCES = ["woq_api.cu", "woq_gemv_w4.cu", "woq_gemv_w4_pro.cu", "woq_gemv_w4_mma.cu", "woq_gemv_w4_mma_pro.cu",
+           "woq_gemv_w6.cu", "woq_gemv_w6_pro.cu", "woq_small_kernels.cu", "woq_pack.cpp", "woq_tree.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

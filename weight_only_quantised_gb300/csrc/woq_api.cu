@@ -254,9 +254,35 @@ int woq_act_quant_int8(const void* x_bf16, int M, int K, int8_t* q, float* ascal
   return launch_act_quant(x_bf16, M, K, q, ascale, (cudaStream_t)stream) == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
 }
 
-static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_bytes, const void* x_bf16,
-                    const int8_t* q, const float* ascale, int M, int N, int K, float* y, void* ws, size_t ws_bytes,
-                    cudaStream_t stream) {
+int woq_rmsnorm_act_quant_int8(const void* x_bf16, const void* gamma_bf16, float eps, int M, int K, int8_t* q,
+                               float* ascale, woq_stream_t stream) {
+  if (M < 0 || M > kMaxM || K < 0 || K % 8 || (size_t)K * 2 > (size_t)max_dynamic_smem()) return WOQ_ERR_SHAPE;
+  if (!(eps >= 0.0f && eps <= 3.4028234e38f)) return WOQ_ERR_SHAPE;
+  if (M == 0) return WOQ_OK;
+  if (!ascale || (K > 0 && (!x_bf16 || !q || !gamma_bf16))) return WOQ_ERR_NULL;
+  if (!aligned(x_bf16, 16) || !aligned(gamma_bf16, 16) || !aligned(q, 16) || !aligned(ascale, 4)) return WOQ_ERR_ALIGN;
+  return launch_pro_act_quant(kern::kProRms, x_bf16, static_cast<const uint16_t*>(gamma_bf16), eps, M, K, q, ascale,
+                              (cudaStream_t)stream) == cudaSuccess
+             ? WOQ_OK
+             : WOQ_ERR_CUDA;
+}
+
+int woq_swiglu_act_quant_int8(const float* gate_up, int M, int K, int8_t* q, float* ascale, woq_stream_t stream) {
+  if (M < 0 || M > kMaxM || K < 0 || K % 8 || (size_t)K * 2 > (size_t)max_dynamic_smem()) return WOQ_ERR_SHAPE;
+  if (M == 0) return WOQ_OK;
+  if (!ascale || (K > 0 && (!gate_up || !q))) return WOQ_ERR_NULL;
+  if (!aligned(gate_up, 16) || !aligned(q, 16) || !aligned(ascale, 4)) return WOQ_ERR_ALIGN;
+  return launch_pro_act_quant(kern::kProSwiglu, gate_up, nullptr, 0.0f, M, K, q, ascale, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? WOQ_OK
+             : WOQ_ERR_CUDA;
+}
+
+// pro: kern::Prologue.  x: bf16 [M][K] (bf16, RMSNorm) or fp32 [M][2K] (SwiGLU).
+static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes, const void* x, const int8_t* q,
+                    const float* ascale, const uint16_t* gamma, float eps, int M, int N, int K, float* y, void* ws,
+                    size_t ws_bytes, cudaStream_t stream) {
+  const bool fused = pro != kern::kProInt8;
   if (M < 0 || M > max_m_for(bits) || N < 0 || K < 0 || K % kGroup || (long)M * K > kMaxMK) return WOQ_ERR_SHAPE;
   if (M == 0 || N == 0) return WOQ_OK;  // nothing to compute
   if (!y) return WOQ_ERR_NULL;
@@ -265,9 +291,12 @@ static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_by
     return cudaMemsetAsync(y, 0, (size_t)M * N * sizeof(float), stream) == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
   }
   if (!wpacked || !ws) return WOQ_ERR_NULL;
-  if (fused ? !x_bf16 : (!q || !ascale)) return WOQ_ERR_NULL;
+  if (fused ? !x : (!q || !ascale)) return WOQ_ERR_NULL;
+  if (pro == kern::kProRms && !gamma) return WOQ_ERR_NULL;
+  if (pro == kern::kProRms && !(eps >= 0.0f && eps <= 3.4028234e38f)) return WOQ_ERR_SHAPE;
   if (!aligned(wpacked, 16) || !aligned(y, 4) || !aligned(ws, 16)) return WOQ_ERR_ALIGN;
-  if (fused ? !aligned(x_bf16, 16) : (!aligned(q, 16) || !aligned(ascale, 4))) return WOQ_ERR_ALIGN;
+  if (fused ? !aligned(x, 16) : (!aligned(q, 16) || !aligned(ascale, 4))) return WOQ_ERR_ALIGN;
+  if (pro == kern::kProRms && !aligned(gamma, 16)) return WOQ_ERR_ALIGN;
   if (wpacked_bytes < packed_bytes(bits, N, K)) return WOQ_ERR_LAYOUT;
   const LaunchConfig cfg = choose_config(bits, M, N, K, fused);
   if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
@@ -275,7 +304,9 @@ static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_by
   if (ws_bytes < wl.total || cfg.ctas > max_ctas_for_workspace()) return WOQ_ERR_WORKSPACE;
   GemvParams p;
   p.w = static_cast<const uint8_t*>(wpacked);
-  p.x = static_cast<const uint16_t*>(x_bf16);
+  p.x = x;
+  p.gamma = gamma;
+  p.eps = eps;
   p.q = q;
   p.ascale = ascale;
   p.y = y;
@@ -296,31 +327,58 @@ static int run_gemv(int bits, bool fused, const void* wpacked, size_t wpacked_by
   p.red_offset = red_offset(M, K, fused, cfg.consumer);
   p.ring_offset = ring_offset(M, K, fused, cfg.consumer);
   p.launch_id = g_launch_counter.fetch_add(1, std::memory_order_relaxed) & 0x7fffffff;
-  const cudaError_t e =
-      bits == 4 ? launch_gemv_w4(fused, cfg.consumer, M, p, cfg, stream) : launch_gemv_w6(fused, M, p, cfg, stream);
+  const cudaError_t e = launch_gemv_any(bits, pro, cfg.consumer, M, p, cfg, stream);
   return e == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
 }
 
 int woq_w4a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
                   int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream) {
-  return run_gemv(4, false, wpacked, wpacked_bytes, nullptr, q, ascale, M, N, K, y, ws, ws_bytes, (cudaStream_t)stream);
+  return run_gemv(4, kern::kProInt8, wpacked, wpacked_bytes, nullptr, q, ascale, nullptr, 0.0f, M, N, K, y, ws,
+                  ws_bytes, (cudaStream_t)stream);
 }
 
 int woq_w6a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
                   int K, float* y, void* ws, size_t ws_bytes, woq_stream_t stream) {
-  return run_gemv(6, false, wpacked, wpacked_bytes, nullptr, q, ascale, M, N, K, y, ws, ws_bytes, (cudaStream_t)stream);
+  return run_gemv(6, kern::kProInt8, wpacked, wpacked_bytes, nullptr, q, ascale, nullptr, 0.0f, M, N, K, y, ws,
+                  ws_bytes, (cudaStream_t)stream);
 }
 
 int woq_w4a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K, float* y,
                          void* ws, size_t ws_bytes, woq_stream_t stream) {
-  return run_gemv(4, true, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, M, N, K, y, ws, ws_bytes,
-                  (cudaStream_t)stream);
+  return run_gemv(4, kern::kProBf16, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, nullptr, 0.0f, M, N, K, y, ws,
+                  ws_bytes, (cudaStream_t)stream);
 }
 
 int woq_w6a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K, float* y,
                          void* ws, size_t ws_bytes, woq_stream_t stream) {
-  return run_gemv(6, true, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, M, N, K, y, ws, ws_bytes,
-                  (cudaStream_t)stream);
+  return run_gemv(6, kern::kProBf16, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, nullptr, 0.0f, M, N, K, y, ws,
+                  ws_bytes, (cudaStream_t)stream);
+}
+
+int woq_w4a8_linear_rmsnorm_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, const void* gamma_bf16,
+                                 float eps, int M, int N, int K, float* y, void* ws, size_t ws_bytes,
+                                 woq_stream_t stream) {
+  return run_gemv(4, kern::kProRms, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr,
+                  static_cast<const uint16_t*>(gamma_bf16), eps, M, N, K, y, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int woq_w6a8_linear_rmsnorm_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, const void* gamma_bf16,
+                                 float eps, int M, int N, int K, float* y, void* ws, size_t ws_bytes,
+                                 woq_stream_t stream) {
+  return run_gemv(6, kern::kProRms, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr,
+                  static_cast<const uint16_t*>(gamma_bf16), eps, M, N, K, y, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int woq_w4a8_linear_swiglu_f32(const void* wpacked, size_t wpacked_bytes, const float* gate_up, int M, int N, int K,
+                               float* y, void* ws, size_t ws_bytes, woq_stream_t stream) {
+  return run_gemv(4, kern::kProSwiglu, wpacked, wpacked_bytes, gate_up, nullptr, nullptr, nullptr, 0.0f, M, N, K, y,
+                  ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int woq_w6a8_linear_swiglu_f32(const void* wpacked, size_t wpacked_bytes, const float* gate_up, int M, int N, int K,
+                               float* y, void* ws, size_t ws_bytes, woq_stream_t stream) {
+  return run_gemv(6, kern::kProSwiglu, wpacked, wpacked_bytes, gate_up, nullptr, nullptr, nullptr, 0.0f, M, N, K, y,
+                  ws, ws_bytes, (cudaStream_t)stream);
 }
 
 int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_bytes, const int8_t* q, int M, int N, int K,
@@ -394,8 +452,8 @@ int woq_w4a8_linear_bf16_noalloc(const void* wpacked, size_t wpacked_bytes, cons
   if (st != WOQ_OK) return st;
   // the array keeps the previous call's contents: start from zero (no allocation involved)
   if (cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream) != cudaSuccess) return WOQ_ERR_CUDA;
-  return run_gemv(4, true, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, M, N, K, y, ws, kNoAllocScratchBytes,
-                  (cudaStream_t)stream);
+  return run_gemv(4, kern::kProBf16, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, nullptr, 0.0f, M, N, K, y, ws,
+                  kNoAllocScratchBytes, (cudaStream_t)stream);
 }
 
 }  // extern "C"

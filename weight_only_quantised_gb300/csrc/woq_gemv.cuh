@@ -50,13 +50,16 @@
 
 #include "woq_device.cuh"
 #include "woq_layout.h"
+#include "woq_prologue.cuh"
 #include "woq_scale_table.h"
 
 namespace woq {
 
 struct GemvParams {
   const uint8_t* w;         // packed buffer (header first)
-  const uint16_t* x;        // bf16 bits [M][K] (fused entry)
+  const void* x;            // bf16 bits [M][K] (bf16 and RMSNorm entries) or fp32 [M][2K] (SwiGLU entry)
+  const uint16_t* gamma;    // bf16 bits [K] (RMSNorm entry)
+  float eps;                // RMSNorm epsilon
   const int8_t* q;          // int8 [M][K] (int8 entry)
   const float* ascale;      // fp32 [M] (int8 entry)
   float* y;                 // fp32 [M][N]
@@ -631,12 +634,107 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
   }
 }
 
+// Prologue of a kernel instance: what the launch receives as activations.
+//   kProInt8:   int8 q [M][K] and fp32 scales [M] (act_quant run before);
+//   kProBf16:   bf16 x [M][K], quantised by the consumer warps (the fused entry);
+//   kProRms:    bf16 x [M][K] and bf16 gamma [K]: RMSNorm, then quantisation;
+//   kProSwiglu: the fp32 [M][2K] output of a gate+up linear: SwiGLU, then quantisation.
+enum Prologue { kProInt8 = 0, kProBf16 = 1, kProRms = 2, kProSwiglu = 3 };
+
+// RMSNorm of the bf16 rows at act (landed by the bulk copy), in place, by the consumer
+// warps (see woq_prologue.cuh for the definition).  s_bits[M]: row max |x| bits, s_sum[M]:
+// integer sums of squares, both zero on entry; shared-memory atomics make both
+// independent of the order the warps arrive in.
+template <int M>
+__device__ __forceinline__ void rmsnorm_prologue(uint8_t* act, int K, const uint16_t* __restrict__ gamma, float eps,
+                                                 int tid, int lane, uint32_t* s_bits, unsigned long long* s_sum) {
+  constexpr int kStride = kConsumers * 8;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(act);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    uint32_t acc = 0;
+    for (int k = 8 * tid; k < K; k += kStride) acc = absmax8(acc, *reinterpret_cast<const uint4*>(xs + m * K + k));
+    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(dev::bf16x2_absmax_to_float(acc)));
+    if (lane == 0) atomicMax(s_bits + m, wm);
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+  int C[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    C[m] = pro::rms_row_exponent(s_bits[m]);
+    unsigned long long part = 0;
+    if (C[m] != -1000) {
+      for (int k = 8 * tid; k < K; k += kStride) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xs + m * K + k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) part += pro::rms_term(w[i] & 0xFFFFu, C[m]) + pro::rms_term(w[i] >> 16, C[m]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0 && part) atomicAdd(s_sum + m, part);
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);  // every x read before the first h write
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const float r = C[m] == -1000 ? 0.0f : pro::rms_rcp(s_sum[m], C[m], K, eps);
+    for (int k = 8 * tid; k < K; k += kStride) {
+      uint4* px = reinterpret_cast<uint4*>(xs + m * K + k);
+      *px = pro::rms_h8(*px, __ldg(reinterpret_cast<const uint4*>(gamma + k)), r);
+    }
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+}
+
+// SwiGLU of the fp32 gate+up rows in global memory into bf16 h at act [M][K].
+template <int M>
+__device__ __forceinline__ void swiglu_prologue(uint8_t* act, int K, const float* __restrict__ gu, int tid) {
+  constexpr int kStride = kConsumers * 8;
+  uint16_t* hs = reinterpret_cast<uint16_t*>(act);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const float* g = gu + (size_t)m * 2 * K;
+    const float* u = g + K;
+    for (int k0 = 8 * tid; k0 < K; k0 += 2 * kStride) {
+      float4 gv[2][2], uv[2][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // two vectors' loads in flight before the arithmetic
+        const int k = k0 + h * kStride;
+        if (k < K) {
+          gv[h][0] = __ldg(reinterpret_cast<const float4*>(g + k));
+          gv[h][1] = __ldg(reinterpret_cast<const float4*>(g + k + 4));
+          uv[h][0] = __ldg(reinterpret_cast<const float4*>(u + k));
+          uv[h][1] = __ldg(reinterpret_cast<const float4*>(u + k + 4));
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int k = k0 + h * kStride;
+        if (k < K) {
+          const float gg[8] = {gv[h][0].x, gv[h][0].y, gv[h][0].z, gv[h][0].w,
+                               gv[h][1].x, gv[h][1].y, gv[h][1].z, gv[h][1].w};
+          const float uu[8] = {uv[h][0].x, uv[h][0].y, uv[h][0].z, uv[h][0].w,
+                               uv[h][1].x, uv[h][1].y, uv[h][1].z, uv[h][1].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            o[i] = pro::swiglu_bf16(gg[2 * i], uu[2 * i]) | (pro::swiglu_bf16(gg[2 * i + 1], uu[2 * i + 1]) << 16);
+          *reinterpret_cast<uint4*>(hs + m * K + k) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+}
+
 // Consumer of a kernel instance: every consumer warp on dp4a, or every one on the f16
 // tensor-core MMA.
 enum Consumer { kDp4a = 0, kMma = 1 };
 
-template <int BITS, int M, bool FUSED, int CONS>
+template <int BITS, int M, int PRO, int CONS>
 __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 288 threads x 112 fit one SM
+  constexpr bool FUSED = PRO != kProInt8;  // activations quantised inside this launch
   static_assert(CONS == kDp4a || BITS == 4, "the tensor-core consumer reads int4 blocks");
   static_assert(CONS == kMma || M <= kMaxMDp4a, "dp4a kernels take up to four activation rows");
   constexpr int BB = Fmt<BITS>::kBlockBytes;
@@ -648,6 +746,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   volatile int* s_flags = reinterpret_cast<volatile int*>(smem + 136);  // [0] ticket-last, [1] abort, [2] header-ok
   float* s_as = reinterpret_cast<float*>(smem + 160);          // [M] activation scales
   float* s_scratch = reinterpret_cast<float*>(smem + 192);     // [8 rows][8 warps] amax partials, to byte 448
+  unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(smem + 448);  // [8] RMSNorm sums of squares
   uint8_t* act = smem + p.act_offset;                          // bf16 x, quantised in place (fused) or int8 q
   float* red = reinterpret_cast<float*>(smem + p.red_offset);  // [4 blocks][M][128 rows]
   uint8_t* ring = smem + p.ring_offset;
@@ -673,6 +772,12 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
     s_flags[1] = 0;
     s_flags[2] = 1;
     dev::fence_mbar_init();
+  }
+  if constexpr (PRO == kProRms) {
+    if (tid < 8) {
+      reinterpret_cast<uint32_t*>(s_scratch)[tid] = 0u;
+      s_sum[tid] = 0ull;
+    }
   }
   __syncthreads();
   if (tid == 0) WOQ_TRACE_EV(0);
@@ -794,10 +899,13 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   if (tid == 0) {
     WOQ_TRACE_EV(3);
     const uint32_t act_bytes = (uint32_t)(FUSED ? 2 * M * p.K : M * p.K);
-    dev::mbar_arrive_expect_tx(actbar, act_bytes);
-    if (FUSED || p.act_stride == p.K) {
-      dev::bulk_copy_g2s(act, FUSED ? static_cast<const void*>(p.x) : static_cast<const void*>(p.q), act_bytes, actbar);
+    if (PRO == kProSwiglu) {
+      dev::mbar_arrive(actbar);  // nothing to copy: the consumers read the fp32 rows themselves
+    } else if (FUSED || p.act_stride == p.K) {
+      dev::mbar_arrive_expect_tx(actbar, act_bytes);
+      dev::bulk_copy_g2s(act, FUSED ? p.x : static_cast<const void*>(p.q), act_bytes, actbar);
     } else {
+      dev::mbar_arrive_expect_tx(actbar, act_bytes);
       for (int m = 0; m < M; ++m)
         dev::bulk_copy_g2s(act + m * p.act_stride, p.q + (size_t)m * p.K, (uint32_t)p.K, actbar);
     }
@@ -823,6 +931,9 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
       atomicOr(p.status, 0x1u /* WOQ_DEVERR_HEADER */);
     }
   }
+  if constexpr (PRO == kProRms)
+    rmsnorm_prologue<M>(act, p.K, p.gamma, p.eps, tid, lane, reinterpret_cast<uint32_t*>(s_scratch), s_sum);
+  if constexpr (PRO == kProSwiglu) swiglu_prologue<M>(act, p.K, static_cast<const float*>(p.x), tid);
   if constexpr (FUSED) {
     quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
                          p.launch_id);

@@ -3,10 +3,17 @@
 
 namespace woq {
 
-cudaError_t launch_gemv_w4(bool fused, int cons, int M, const GemvParams& p, const LaunchConfig& cfg,
-                           cudaStream_t stream) {
-  if (cons != kern::kDp4a) return launch_gemv_w4_mma(fused, cons, M, p, cfg, stream);
-  return launch_gemv_bits<4, kern::kDp4a>(fused, M, p, cfg, stream);
+cudaError_t launch_w4_dp4a_plain(int pro, int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream) {
+  return launch_gemv_pair<4, kern::kDp4a, kern::kProInt8, kern::kProBf16>(pro, M, p, cfg, stream);
+}
+
+cudaError_t launch_gemv_any(int bits, int pro, int cons, int M, const GemvParams& p, const LaunchConfig& cfg,
+                            cudaStream_t stream) {
+  const bool plain = pro == kern::kProInt8 || pro == kern::kProBf16;
+  if (bits == 6) return plain ? launch_w6_plain(pro, M, p, cfg, stream) : launch_w6_norm(pro, M, p, cfg, stream);
+  if (cons == kern::kMma)
+    return plain ? launch_w4_mma_plain(pro, M, p, cfg, stream) : launch_w4_mma_norm(pro, M, p, cfg, stream);
+  return plain ? launch_w4_dp4a_plain(pro, M, p, cfg, stream) : launch_w4_dp4a_norm(pro, M, p, cfg, stream);
 }
 
 }  // namespace woq

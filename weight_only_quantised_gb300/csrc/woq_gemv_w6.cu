@@ -1,10 +1,10 @@
-// Instantiations of the skinny GEMV / linear kernel for int6 weights.
+// Instantiations of the skinny GEMV / linear for int6 weights (dp4a), int8 and bf16 prologues.
 #include "woq_gemv_launch.cuh"
 
 namespace woq {
 
-cudaError_t launch_gemv_w6(bool fused, int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream) {
-  return launch_gemv_bits<6, kern::kDp4a>(fused, M, p, cfg, stream);
+cudaError_t launch_w6_plain(int pro, int M, const GemvParams& p, const LaunchConfig& cfg, cudaStream_t stream) {
+  return launch_gemv_pair<6, kern::kDp4a, kern::kProInt8, kern::kProBf16>(pro, M, p, cfg, stream);
 }
 
 }  // namespace woq

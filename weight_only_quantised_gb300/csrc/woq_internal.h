@@ -43,6 +43,9 @@ cudaError_t launch_gemv(int bits, bool fused, int M, int N, int K, const void* w
                         const int8_t* q, const float* ascale, float* y, void* ws, const LaunchConfig& cfg,
                         const WorkspaceLayout& wl, cudaStream_t stream);
 cudaError_t launch_act_quant(const void* x_bf16, int M, int K, int8_t* q, float* ascale, cudaStream_t stream);
+// pro: kern::kProRms (x bf16 [M][K], gamma bf16 [K]) or kern::kProSwiglu (x fp32 [M][2K])
+cudaError_t launch_pro_act_quant(int pro, const void* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q,
+                                 float* ascale, cudaStream_t stream);
 cudaError_t launch_group_dots(int bits, const void* wpacked, const int8_t* q, int M, int N, int K, int32_t* dots,
                               cudaStream_t stream);
 cudaError_t launch_pack_device(int bits, const uint8_t* q, const uint16_t* scales, int N, int K, void* dst,

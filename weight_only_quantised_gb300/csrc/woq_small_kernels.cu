@@ -74,6 +74,76 @@ __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint16_t* _
 }
 
 // ---------------------------------------------------------------------------
+// Standalone RMSNorm / SwiGLU followed by activation quantisation (the unfused
+// form of the linear's prologue fusions, same arithmetic: woq_prologue.cuh).
+// One CTA per row; h is formed in shared memory (bf16 [K]) and quantised as by
+// act_quant_kernel.  K % 8 == 0.
+// ---------------------------------------------------------------------------
+template <int PRO>
+__global__ void __launch_bounds__(kAqThreads) pro_act_quant_kernel(const void* __restrict__ x,
+                                                                   const uint16_t* __restrict__ gamma, float eps,
+                                                                   int K, int8_t* __restrict__ q,
+                                                                   float* __restrict__ ascale) {
+  extern __shared__ __align__(16) uint16_t s_h[];  // [K]
+  __shared__ float s_part[kAqThreads / 32];
+  __shared__ uint32_t s_bits;
+  __shared__ unsigned long long s_sum;
+  dev::pdl_launch_dependents();
+  dev::pdl_wait_prior_grids();
+  const int m = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (PRO == kProRms) {
+    const uint16_t* xr = static_cast<const uint16_t*>(x) + (size_t)m * K;
+    if (tid == 0) {
+      s_bits = 0u;
+      s_sum = 0ull;
+    }
+    __syncthreads();
+    uint32_t acc = 0;
+    for (int e = tid * 8; e < K; e += kAqThreads * 8) acc = absmax8(acc, __ldg(reinterpret_cast<const uint4*>(xr + e)));
+    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(dev::bf16x2_absmax_to_float(acc)));
+    if (lane == 0) atomicMax(&s_bits, wm);
+    __syncthreads();
+    const int C = pro::rms_row_exponent(s_bits);
+    unsigned long long part = 0;
+    if (C != -1000) {
+      for (int e = tid * 8; e < K; e += kAqThreads * 8) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + e));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) part += pro::rms_term(w[i] & 0xFFFFu, C) + pro::rms_term(w[i] >> 16, C);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0 && part) atomicAdd(&s_sum, part);
+    __syncthreads();
+    const float r = C == -1000 ? 0.0f : pro::rms_rcp(s_sum, C, K, eps);
+    for (int e = tid * 8; e < K; e += kAqThreads * 8)
+      *reinterpret_cast<uint4*>(s_h + e) = pro::rms_h8(__ldg(reinterpret_cast<const uint4*>(xr + e)),
+                                                       __ldg(reinterpret_cast<const uint4*>(gamma + e)), r);
+  } else {
+    const float* g = static_cast<const float*>(x) + (size_t)m * 2 * K;
+    const float* u = g + K;
+    for (int e = tid; e < K; e += kAqThreads) s_h[e] = (uint16_t)pro::swiglu_bf16(__ldg(g + e), __ldg(u + e));
+  }
+  __syncthreads();
+  // quantise h as act_quant_kernel quantises x
+  float amax = 0.0f;
+  for (int e = tid; e < K; e += kAqThreads) amax = fmaxf(amax, fabsf(dev::bf16_bits_to_float(s_h[e])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) s_part[tid >> 5] = amax;
+  __syncthreads();
+  amax = s_part[0];
+  for (int i = 1; i < kAqThreads / 32; ++i) amax = fmaxf(amax, s_part[i]);
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (tid == 0) ascale[m] = s;
+  int8_t* qr = q + (size_t)m * K;
+  for (int e = tid; e < K; e += kAqThreads) qr[e] = quant_one(dev::bf16_bits_to_float(s_h[e]), s);
+}
+
+// ---------------------------------------------------------------------------
 // Debug: exact per-group dot products straight from the packed layout.
 // One thread per (row n, group g); dots[m][n][g].
 // ---------------------------------------------------------------------------
@@ -213,6 +283,29 @@ cudaError_t launch_act_quant(const void* x_bf16, int M, int K, int8_t* q, float*
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   void* args[] = {(void*)&x, (void*)&K, (void*)&q, (void*)&ascale};
   return launch_pdl((const void*)kern::act_quant_kernel, dim3((unsigned)M), dim3(kern::kAqThreads), stream, args);
+}
+
+cudaError_t launch_pro_act_quant(int pro, const void* x, const uint16_t* gamma, float eps, int M, int K, int8_t* q,
+                                 float* ascale, cudaStream_t stream) {
+  const void* func = pro == kern::kProRms ? (const void*)kern::pro_act_quant_kernel<kern::kProRms>
+                                          : (const void*)kern::pro_act_quant_kernel<kern::kProSwiglu>;
+  const size_t smem = (size_t)K * 2;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  void* args[] = {(void*)&x, (void*)&gamma, (void*)&eps, (void*)&K, (void*)&q, (void*)&ascale};
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)M);
+  lc.blockDim = dim3(kern::kAqThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelExC(&lc, func, args);
 }
 
 template <int BITS>
