@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--m", type=int, default=1, help="activation rows of the headline step")
     ap.add_argument("--extra-m", default="3,4", help="also time the step at these M (comma list, '' for none)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prologue-fusion", dest="prologue_fusion", action="store_false",
+                    help="skip the RMSNorm / SwiGLU prologue-fusion step (fused against unfused)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-div", type=int, default=8, help="oracle sample: 1/div of every linear's rows")
     ap.add_argument("--linear", default="", help="time one 27B-class linear (qkv, o, gate_up, down, lm_head) "
@@ -191,6 +193,59 @@ class Step:
         for (name, K, N), p in zip(self.linears, self.packed):
             woq.woq_w4a8_linear_bf16(p, xs[K], N, K, ys[N], ws)
 
+    def time_prologue_chain(self, M, steps, warmup, fused):
+        """The step as a dependency chain with the prologue fusions of "Optimizing the Linear
+        Kernel": qkv and gate_up behind an RMSNorm, down behind the SwiGLU of the gate_up output
+        (its fp32 y is the down projection's input), o on the bf16 entry, the LM head behind
+        the final RMSNorm.  fused: one launch per linear; else the unfused twins
+        (woq_rmsnorm_act_quant_int8 / woq_swiglu_act_quant_int8) then the int8 GEMV."""
+        torch, synthetic, woq = self.torch, self.synthetic, self.woq
+        xs, ys, ws = self.buffers(M)
+        K = 5120
+        gamma = synthetic.rmsnorm_weight(K, 9, device=self.device)
+        qs = {Kl: torch.empty((M, Kl), dtype=torch.int8, device=self.device) for Kl in (5120, 17408)}
+        a = torch.empty((M,), dtype=torch.float32, device=self.device)
+
+        def launch():
+            for (name, Kl, N), p in zip(self.linears, self.packed):
+                kind = name.split(".")[-1]
+                y = ys[N]
+                if kind in ("qkv", "gate_up", "lm_head"):
+                    if fused:
+                        woq.woq_w4a8_linear_rmsnorm_bf16(p, xs[Kl], gamma, 1e-6, N, Kl, y, ws)
+                    else:
+                        woq.woq_rmsnorm_act_quant_int8(xs[Kl], gamma, 1e-6, qs[Kl], a)
+                        woq.woq_w4a8_gemv(p, qs[Kl], a, N, Kl, y, ws)
+                elif kind == "down":
+                    gu = ys[2 * Kl]  # the gate_up output of this layer
+                    if fused:
+                        woq.woq_w4a8_linear_swiglu_f32(p, gu, N, Kl, y, ws)
+                    else:
+                        woq.woq_swiglu_act_quant_int8(gu, qs[Kl], a)
+                        woq.woq_w4a8_gemv(p, qs[Kl], a, N, Kl, y, ws)
+                else:
+                    woq.woq_w4a8_linear_bf16(p, xs[Kl], N, Kl, y, ws)
+
+        stream = torch.cuda.Stream(device=self.device)
+        ys[34816].zero_()
+        with torch.cuda.stream(stream):
+            launch()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch()
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        assert self.woq.woq_read_status(ws) == 0
+        return e0.elapsed_time(e1) / steps
+
     def capture(self, M):
         torch = self.torch
         xs, ys, ws = self.buffers(M)
@@ -322,6 +377,15 @@ def run_ours(args):
                            "gbs": round(b_e / (ms_e * 1e-3) / 1e9, 1),
                            "vs_m1_time": round(ms_e / ms_step, 4)}
 
+    prologue = None
+    if args.prologue_fusion:
+        k = min(args.steps, 200)
+        f_ms = max_over_ranks(step.time_prologue_chain(M, k, min(args.warmup, 5), fused=True))
+        u_ms = max_over_ranks(step.time_prologue_chain(M, k, min(args.warmup, 5), fused=False))
+        prologue = {"fused_ms_per_step": round(f_ms, 4), "unfused_ms_per_step": round(u_ms, 4),
+                    "fused_launches": len(step.linears), "unfused_launches": len(step.linears) + 3 * 64 + 1,
+                    "what": "qkv, gate_up, lm_head behind RMSNorm; down behind SwiGLU of the gate_up output"}
+
     e2e = None
     if not args.no_e2e:
         k = min(args.steps, 200)
@@ -364,6 +428,7 @@ def run_ours(args):
                      "peak_kind": peak_kind, "kernel": "woq::kern::gemv_kernel<4, M, fused, dp4a>",
                      "per": "step (257 launches)"},
         "extra_m": extra,
+        "prologue_fusion": prologue,
         "e2e": e2e,
         "gpu_launches": len(step.linears) * args.steps,
         "clocks": clocks,
