@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--int8", action="store_true", help="with --linear: the int8 entry (act_quant once, then GEMV)")
     ap.add_argument("--tree-planner", action="store_true",
                     help="time one re-plan of the draft-tree planner (host code) against its oracle")
+    ap.add_argument("--relayout", action="store_true",
+                    help="time the in-place relayout of 27B-class matrices instead of the step")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
                     help="with --linear: int4 consumer (0 launch table, 1 dp4a, 2 tensor-core MMA)")
     return ap.parse_args()
@@ -597,10 +599,63 @@ def run_tree_planner(args):
                                        "sample": f"{m} re-plans"}}), flush=True)
 
 
+def run_relayout(args):
+    """In-place relayout (woq_relayout_inplace) of 27B-class int4 / int6 matrices, timed per call
+    with CUDA events; beside it the out-of-place device packer (woq_pack_device) on the same input."""
+    import torch
+
+    import synthetic
+    import weight_only_quantised_gb300 as woq
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = measured_peak()
+    rows = []
+    for bits, name, (K, N) in [(4, "gate_up", synthetic.LINEARS_27B["gate_up"]), (4, "lm_head", synthetic.LM_HEAD_27B),
+                               (6, "gate_up", synthetic.LINEARS_27B["gate_up"])]:
+        w, s = synthetic.weights(bits, N, K, seed=9, device=dev)
+        nbytes = woq.woq_packed_bytes(bits, N, K)
+        buf = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+        ref = torch.empty_like(buf)
+        algo = w.numel() + 2 * s.numel() + nbytes  # canonical bytes read + packed bytes written
+        times = {"relayout_inplace": [], "pack_device": []}
+        for it in range(args.warmup + max(3, min(args.steps, 10))):
+            woq.canonical_into_buffer(bits, w, s.view(torch.int16), buf)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            woq.woq_relayout_inplace(bits, buf, N, K)
+            b.record()
+            torch.cuda.synchronize()
+            c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c.record()
+            woq.woq_pack_device(bits, w, s.view(torch.int16), N, K, ref)
+            d.record()
+            torch.cuda.synchronize()
+            if it >= args.warmup:
+                times["relayout_inplace"].append(a.elapsed_time(b))
+                times["pack_device"].append(c.elapsed_time(d))
+        assert torch.equal(buf, ref), "relayout differs from the device packer"
+        row = {"matrix": f"27B {name} int{bits} (N={N}, K={K})", "algorithmic_bytes": algo}
+        for key, v in times.items():
+            ms = float(statistics.median(v))
+            row[key] = {"ms": round(ms, 4), "gbs": round(algo / (ms * 1e-3) / 1e9, 1),
+                        "frac": round(algo / (ms * 1e-3) / 1e9 / peak, 4)}
+        rows.append(row)
+        del w, s, buf, ref
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "in-place relayout throughput", "unit": "GB/s", "higher_is_better": True,
+                      "peak": peak, "peak_kind": peak_kind, "rows": rows,
+                      "note": "median over calls; woq_relayout_inplace includes its header memset and "
+                              "read-back; pack_device writes into a second buffer"}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.tree_planner:
         run_tree_planner(args)
+        return
+    if args.relayout:
+        run_relayout(args)
         return
     if args.linear:
         run_linear(args)

@@ -126,6 +126,23 @@ WOQ_API int woq_unpack(int bits, const void* packed, size_t packed_bytes, int N,
 WOQ_API int woq_pack_device(int bits, const uint8_t* q_dev, const uint16_t* scales_dev, int N, int K, void* dst_dev,
                     size_t dst_bytes, woq_stream_t stream);
 
+/* In-place device relayout ("Doubling LLM token rates in ComfyUI", section
+ * "Optimizing the Linear Kernel": the weights are re-laid out in VRAM in place,
+ * once per load, with no extra RAM or VRAM).  buf (device, 16-byte aligned, at
+ * least woq_packed_bytes(bits, N, K) bytes) holds on entry, from byte 256 on, the
+ * canonical weights of all N rows (N * row bytes) directly followed by the
+ * canonical fp16 scales (N * K/128 uint16); bytes 0 .. 255 and everything after
+ * the scales are scratch.  On return buf holds exactly what woq_pack_device
+ * would have written.  No device or host memory is allocated (bytes 0 .. 255
+ * serve as the kernel's barrier words until the header is written last).
+ * Synchronous: waits for the stream, then reads the header back.  Errors:
+ * WOQ_ERR_NULL, WOQ_ERR_ALIGN, WOQ_ERR_LAYOUT (buf_bytes too small), WOQ_ERR_SHAPE
+ * (bad shape, or more group scales than the SMs' shared memory can stage:
+ * about 16 million on a 152-SM GPU), WOQ_ERR_CUDA (cooperative launch unsupported or failed), WOQ_ERR_DEVICE
+ * (a barrier wait ran out: the contents of buf are then undefined and its header
+ * invalid, so no GEMV accepts it). */
+WOQ_API int woq_relayout_inplace(int bits, void* buf, size_t buf_bytes, int N, int K, woq_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Workspace.  GEMV / linear launches split the weight stream evenly over the
  * GPU's SMs; a 128-row tile that straddles CTAs is finished by one of them,

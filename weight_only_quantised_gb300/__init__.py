@@ -50,6 +50,7 @@ _SIGS = {
     "woq_pack_w6": ([_P, _P, _I, _I, _P, _Z], _I),
     "woq_unpack": ([_I, _P, _Z, _I, _I, _P, _P], _I),
     "woq_pack_device": ([_I, _P, _P, _I, _I, _P, _Z, _P], _I),
+    "woq_relayout_inplace": ([_I, _P, _Z, _I, _I, _P], _I),
     "woq_workspace_bytes": ([_I, _I, _I, _I], _Z),
     "woq_workspace_init": ([_P, _Z, _P], _I),
     "woq_read_status": ([_P, _Z, _I, ctypes.POINTER(ctypes.c_uint32), _P], _I),
@@ -162,6 +163,23 @@ def woq_pack_device(bits: int, q_dev, scales_dev, N: int, K: int, dst_dev, strea
     """Device pack into dst_dev (uint8 tensor of woq_packed_bytes(bits, N, K) bytes)."""
     _check(lib.woq_pack_device(bits, _dptr(q_dev), _dptr(scales_dev), N, K, _dptr(dst_dev), _nbytes(dst_dev),
                                _stream(stream)), "woq_pack_device")
+
+
+def woq_relayout_inplace(bits: int, buf, N: int, K: int, stream=None) -> None:
+    """In-place relayout of buf (uint8 device tensor of woq_packed_bytes(bits, N, K)
+    bytes): canonical weights from byte 256 on, then the fp16 scales; packed on return."""
+    _check(lib.woq_relayout_inplace(bits, _dptr(buf), _nbytes(buf), N, K, _stream(stream)),
+           "woq_relayout_inplace")
+
+
+def canonical_into_buffer(bits: int, q_dev, scales_dev, buf) -> None:
+    """Place canonical weights and scales (device tensors) where woq_relayout_inplace expects them."""
+    import torch
+
+    qb = q_dev.reshape(-1).view(torch.uint8)
+    sb = scales_dev.reshape(-1).view(torch.uint8)
+    buf[256:256 + qb.numel()].copy_(qb)
+    buf[256 + qb.numel():256 + qb.numel() + sb.numel()].copy_(sb)
 
 
 # ----------------------------------------------------------------------------- workspace

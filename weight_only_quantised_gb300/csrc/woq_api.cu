@@ -246,6 +246,29 @@ int woq_pack_device(int bits, const uint8_t* q_dev, const uint16_t* scales_dev, 
              : WOQ_ERR_CUDA;
 }
 
+int woq_relayout_inplace(int bits, void* buf, size_t buf_bytes, int N, int K, woq_stream_t stream) {
+  const size_t need = packed_bytes(bits, N, K);
+  if (need == 0) return WOQ_ERR_SHAPE;
+  if (!buf) return WOQ_ERR_NULL;
+  if (!aligned(buf, 16)) return WOQ_ERR_ALIGN;
+  if (buf_bytes < need) return WOQ_ERR_LAYOUT;
+  if (N == 0 || K == 0) {  // nothing to move: the header alone
+    alignas(16) uint8_t h[kHeaderBytes];
+    write_header(h, bits, N, K);
+    cudaError_t e = cudaMemcpyAsync(buf, h, kHeaderBytes, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    return e == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+  }
+  int too_large = 0;
+  cudaError_t e = launch_relayout(bits, buf, N, K, &too_large, (cudaStream_t)stream);
+  if (too_large) return WOQ_ERR_SHAPE;
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  uint32_t head[4] = {0u, 0u, 0u, 0u};
+  if (e == cudaSuccess) e = cudaMemcpy(head, buf, sizeof(head), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return WOQ_ERR_CUDA;
+  return head[0] == kMagic ? WOQ_OK : WOQ_ERR_DEVICE;
+}
+
 int woq_act_quant_int8(const void* x_bf16, int M, int K, int8_t* q, float* ascale, woq_stream_t stream) {
   if (M < 0 || M > kMaxM || K < 0) return WOQ_ERR_SHAPE;
   if (M == 0) return WOQ_OK;

@@ -190,6 +190,60 @@ __global__ void group_dots_kernel(const uint8_t* __restrict__ w, const int8_t* _
 // Device packer: one thread per (tile, group, quarter c, row group j, lane l)
 // chunk; writes the same bytes as the host packer.
 // ---------------------------------------------------------------------------
+__host__ __device__ inline size_t canonical_row_bytes(int bits, int K) {
+  return bits == 4 ? (size_t)K / 2 : (size_t)K / 4 * 3;
+}
+
+// The packed words of one chunk (one row, one 32-k quarter) from its canonical bytes:
+// 16 bytes of int4 (two per byte, low nibble = even k) or 24 bytes of int6 (four per
+// three bytes).  lo: the int4 / low-nibble words, hi: the int6 high-bit words.
+template <int BITS>
+__device__ __forceinline__ void pack_chunk(const uint8_t* __restrict__ src, uint32_t (&lo)[4], uint32_t (&hi)[2]) {
+  uint8_t code[32];
+  if constexpr (BITS == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) code[kk] = (uint8_t)((vw[kk >> 3] >> (4 * (kk & 7))) & 0xF);
+  } else {
+    const uint2 a = *reinterpret_cast<const uint2*>(src);
+    const uint2 b = *reinterpret_cast<const uint2*>(src + 8);
+    const uint2 cc = *reinterpret_cast<const uint2*>(src + 16);
+    const uint32_t bw[6] = {a.x, a.y, b.x, b.y, cc.x, cc.y};
+#pragma unroll
+    for (int quad = 0; quad < 8; ++quad) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int byte = 0; byte < 3; ++byte) {
+        const int pos = quad * 3 + byte;
+        word |= ((bw[pos >> 2] >> (8 * (pos & 3))) & 0xFFu) << (8 * byte);
+      }
+#pragma unroll
+      for (int f = 0; f < 4; ++f) code[quad * 4 + f] = (uint8_t)((word >> (6 * f)) & 0x3F);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    lo[i] = 0u;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint8_t ca = code[8 * i + b], cb = code[8 * i + 4 + b];
+      lo[i] |= ((uint32_t)(ca & 0xF) | ((uint32_t)(cb & 0xF) << 4)) << (8 * b);
+    }
+  }
+  hi[0] = hi[1] = 0u;
+  if constexpr (BITS == 6) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint8_t ca = code[8 * i + b], cb = code[8 * i + 4 + b];
+        const int h = i >> 1, e = i & 1;
+        hi[h] |= ((uint32_t)((ca >> 4) & 3) << (2 * (2 * e))) << (8 * b);
+        hi[h] |= ((uint32_t)((cb >> 4) & 3) << (2 * (2 * e + 1))) << (8 * b);
+      }
+  }
+}
 template <int BITS>
 __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ scales, int N, int K, int T,
                             uint8_t* __restrict__ dst, PackedHeader hdr) {
@@ -215,42 +269,7 @@ __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __res
     uint32_t hi[2] = {0u, 0u};
     if (n < N) {
       const int kb = g * kGroup + 32 * c;
-      uint8_t code[32];
-      if constexpr (BITS == 4) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + (size_t)n * (K / 2) + kb / 2));
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int kk = 0; kk < 32; ++kk) code[kk] = (uint8_t)((vw[kk >> 3] >> (4 * (kk & 7))) & 0xF);
-      } else {
-        const uint8_t* src = q + (size_t)n * (K / 4 * 3) + (size_t)(kb / 4) * 3;
-        const uint2 a = __ldg(reinterpret_cast<const uint2*>(src));
-        const uint2 b = __ldg(reinterpret_cast<const uint2*>(src + 8));
-        const uint2 cc = __ldg(reinterpret_cast<const uint2*>(src + 16));
-        const uint32_t bw[6] = {a.x, a.y, b.x, b.y, cc.x, cc.y};
-#pragma unroll
-        for (int quad = 0; quad < 8; ++quad) {
-          uint32_t word = 0;
-#pragma unroll
-          for (int byte = 0; byte < 3; ++byte) {
-            const int pos = quad * 3 + byte;
-            word |= ((bw[pos >> 2] >> (8 * (pos & 3))) & 0xFFu) << (8 * byte);
-          }
-#pragma unroll
-          for (int f = 0; f < 4; ++f) code[quad * 4 + f] = (uint8_t)((word >> (6 * f)) & 0x3F);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const uint8_t ca = code[8 * i + b], cb = code[8 * i + 4 + b];
-          lo[i] |= ((uint32_t)(ca & 0xF) | ((uint32_t)(cb & 0xF) << 4)) << (8 * b);
-          if constexpr (BITS == 6) {
-            const int h = i >> 1, e = i & 1;
-            hi[h] |= ((uint32_t)((ca >> 4) & 3) << (2 * (2 * e))) << (8 * b);
-            hi[h] |= ((uint32_t)((cb >> 4) & 3) << (2 * (2 * e + 1))) << (8 * b);
-          }
-        }
+      pack_chunk<BITS>(q + (size_t)n * canonical_row_bytes(BITS, K) + (size_t)kb * BITS / 8, lo, hi);
     }
     *reinterpret_cast<uint4*>(blk + w4_chunk_offset(c, j, l)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     if constexpr (BITS == 6)
@@ -260,6 +279,151 @@ __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __res
       const uint16_t s = n < N ? scales[(size_t)n * G + g] : (uint16_t)0;
       reinterpret_cast<uint16_t*>(blk)[scale_index(r)] = s;
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// In-place relayout ("Optimizing the Linear Kernel": the re-layout is done in place in
+// VRAM, once per model load, with no extra RAM or VRAM).  The buffer holds, from byte
+// 256 on, the canonical weights (N rows) directly followed by the canonical fp16 scales;
+// it ends up holding the packed layout.  A packed tile t starts at 256 + t G BB, never
+// below the canonical bytes of any lower tile (G BB >= 128 row bytes), so the tiles are
+// rewritten in batches of whole tiles from the top down: every CTA first copies all the
+// scales it will write into shared memory (the top tiles overwrite the scale region),
+// then per batch gathers its blocks' canonical chunks, converted to the packed order,
+// into shared memory, meets the other CTAs at a grid barrier (every read of the batch is
+// done) and writes them out.  The 256-byte header slot holds the barrier words (0: arrivals,
+// 1: generation, 2: failure, 3: departures) until CTA 0, once every CTA has counted its
+// last write, writes the header over them.  One CTA per SM, launched cooperatively (all
+// resident); every wait is bounded, and a wait that runs out sets word 2 and ends its CTA,
+// so the header is never written.
+// ---------------------------------------------------------------------------
+constexpr int kRlThreads = 512;  // one thread per chunk of a block
+
+struct RelayoutPlan {
+  int N, K, T, G;
+  int tiles_per_batch;  // whole tiles per batch, batches from the top down
+  int q_slots;          // blocks a CTA stages per batch
+  int scale_slots;      // blocks whose scales a CTA stages for the whole run
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid barrier on words[0] (arrivals) and words[1] (generation); bounded.
+__device__ bool rl_grid_barrier(uint32_t* words, int* s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    const uint32_t gen = ld_acquire_u32(words + 1);
+    __threadfence();
+    if (atomicAdd(words, 1u) == gridDim.x - 1) {
+      atomicExch(words, 0u);
+      __threadfence();
+      st_release_u32(words + 1, gen + 1);
+    } else {
+      const uint64_t t0 = dev::global_timer_ns();
+      while (ld_acquire_u32(words + 1) == gen) {
+        if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) {
+          ok = false;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    if (!ok) atomicExch(words + 2, 1u);
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, RelayoutPlan pl, PackedHeader hdr) {
+  constexpr int BB = Fmt<BITS>::kBlockBytes;
+  constexpr int QB = BB - kScaleBytes;  // weight bytes of a block
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* s_scales = reinterpret_cast<uint16_t*>(smem);              // [scale_slots][128], packed order
+  uint8_t* s_q = smem + (size_t)pl.scale_slots * kScaleBytes;          // [q_slots][QB], packed order
+  __shared__ int s_ok;
+  uint32_t* words = reinterpret_cast<uint32_t*>(buf);
+  const uint8_t* canon_q = buf + kHeaderBytes;
+  const size_t R = canonical_row_bytes(BITS, pl.K);
+  const uint16_t* canon_s = reinterpret_cast<const uint16_t*>(canon_q + (size_t)pl.N * R);
+  const int C = (int)gridDim.x, cta = (int)blockIdx.x, tid = (int)threadIdx.x;
+
+  // every scale this CTA will write, in the order it will write them
+  int slot = 0;
+  for (int thi = pl.T; thi > 0; thi -= pl.tiles_per_batch) {
+    const int tlo = thi > pl.tiles_per_batch ? thi - pl.tiles_per_batch : 0;
+    const int nb = (thi - tlo) * pl.G;
+    for (int i = cta; i < nb; i += C, ++slot) {
+      const int b = tlo * pl.G + i, t = b / pl.G, g = b % pl.G;
+      for (int r = tid; r < kTileRows; r += kRlThreads) {
+        const int n = t * kTileRows + r;
+        s_scales[slot * kTileRows + scale_index(r)] = n < pl.N ? canon_s[(size_t)n * pl.G + g] : (uint16_t)0;
+      }
+    }
+  }
+  if (!rl_grid_barrier(words, &s_ok)) return;
+
+  slot = 0;
+  const int l = tid & 31, j = (tid >> 5) & 3, c4 = tid >> 7;  // this thread's chunk of every block
+  for (int thi = pl.T; thi > 0; thi -= pl.tiles_per_batch) {
+    const int tlo = thi > pl.tiles_per_batch ? thi - pl.tiles_per_batch : 0;
+    const int nb = (thi - tlo) * pl.G;
+    int k = 0;
+    for (int i = cta; i < nb; i += C, ++k) {  // gather, converted to the packed order
+      const int b = tlo * pl.G + i, t = b / pl.G, g = b % pl.G;
+      const int n = t * kTileRows + 32 * j + l;
+      uint32_t lo[4] = {0u, 0u, 0u, 0u};
+      uint32_t hi[2] = {0u, 0u};
+      if (n < pl.N) pack_chunk<BITS>(canon_q + (size_t)n * R + (size_t)(g * kGroup + 32 * c4) * BITS / 8, lo, hi);
+      uint8_t* sb = s_q + (size_t)k * QB - kScaleBytes;  // chunk offsets count from the block start
+      *reinterpret_cast<uint4*>(sb + w4_chunk_offset(c4, j, l)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      if constexpr (BITS == 6) *reinterpret_cast<uint2*>(sb + hi_chunk_offset(c4, j, l)) = make_uint2(hi[0], hi[1]);
+    }
+    if (!rl_grid_barrier(words, &s_ok)) return;  // every canonical byte of the batch has been read
+    k = 0;
+    for (int i = cta; i < nb; i += C, ++k, ++slot) {
+      uint8_t* out = buf + kHeaderBytes + (size_t)(tlo * pl.G + i) * BB;
+      for (int e = tid; e < kScaleBytes / 16; e += kRlThreads)
+        reinterpret_cast<uint4*>(out)[e] = reinterpret_cast<const uint4*>(s_scales + (size_t)slot * kTileRows)[e];
+      for (int e = tid; e < QB / 16; e += kRlThreads)
+        reinterpret_cast<uint4*>(out + kScaleBytes)[e] = reinterpret_cast<const uint4*>(s_q + (size_t)k * QB)[e];
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {  // count this CTA's writes as done
+    __threadfence();
+    atomicAdd(words + 3, 1u);
+  }
+  if (cta != 0) return;
+  if (tid == 0) {  // CTA 0 waits for every CTA, so nobody still reads the barrier words
+    bool ok = true;
+    const uint64_t t0 = dev::global_timer_ns();
+    while (ld_acquire_u32(words + 3) != (uint32_t)C) {
+      if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) {
+        ok = false;
+        break;
+      }
+      __nanosleep(128);
+    }
+    if (!ok) atomicExch(words + 2, 1u);
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  if (tid < kHeaderBytes / 4) {  // the header last, over the barrier words
+    uint32_t word = 0;
+    if (tid * 4 < (int)sizeof(PackedHeader)) memcpy(&word, reinterpret_cast<const uint8_t*>(&hdr) + tid * 4, 4);
+    words[tid] = word;
   }
 }
 
@@ -363,6 +527,78 @@ cudaError_t launch_pack_device(int bits, const uint8_t* q, const uint16_t* scale
   else
     kern::pack_kernel<6><<<blocks, threads, 0, stream>>>(q, scales, N, K, T, d, h);
   return cudaGetLastError();
+}
+
+}  // namespace woq
+
+
+namespace woq {
+
+// Relayout plan: batches of whole tiles whose staged blocks fit next to all of the CTA's
+// staged scales; 0 tiles per batch if even one tile does not fit.
+static kern::RelayoutPlan relayout_plan(int bits, int N, int K, int ctas, int smem) {
+  kern::RelayoutPlan pl = {N, K, (N + kTileRows - 1) / kTileRows, K / kGroup, 0, 0, 0};
+  const int QB = block_bytes(bits) - kScaleBytes;
+  for (int tb = pl.T; tb >= 1; --tb) {
+    int scale_slots = 0, q_slots = 0;
+    for (int thi = pl.T; thi > 0; thi -= tb) {
+      const int tlo = thi > tb ? thi - tb : 0;
+      const int per = ((thi - tlo) * pl.G + ctas - 1) / ctas;
+      scale_slots += per;
+      if (per > q_slots) q_slots = per;
+    }
+    if ((long long)scale_slots * kScaleBytes + (long long)q_slots * QB <= smem) {
+      pl.tiles_per_batch = tb;
+      pl.q_slots = q_slots;
+      pl.scale_slots = scale_slots;
+      return pl;
+    }
+  }
+  return pl;
+}
+
+cudaError_t launch_relayout(int bits, void* buf, int N, int K, int* too_large, cudaStream_t stream) {
+  *too_large = 0;
+  int dev = 0, sms = 0, smem = 0, coop = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e != cudaSuccess) return e;
+  if (!coop) return cudaErrorNotSupported;
+  const int budget = smem - 1024;  // static shared memory and slack
+  const kern::RelayoutPlan pl = relayout_plan(bits, N, K, sms, budget);
+  if (pl.tiles_per_batch <= 0) {
+    *too_large = 1;
+    return cudaSuccess;
+  }
+  PackedHeader h;
+  memset(&h, 0, sizeof(h));
+  h.magic = kMagic;
+  h.version = kLayoutVersion;
+  h.bits = (uint32_t)bits;
+  h.tile_rows = kTileRows;
+  h.N = (uint32_t)N;
+  h.K = (uint32_t)K;
+  h.tiles = (uint32_t)pl.T;
+  h.groups = (uint32_t)pl.G;
+  h.block_bytes = (uint64_t)block_bytes(bits);
+  h.total_bytes = (uint64_t)packed_bytes(bits, N, K);
+  const void* func = bits == 4 ? (const void*)kern::relayout_kernel<4> : (const void*)kern::relayout_kernel<6>;
+  const size_t dyn = (size_t)pl.scale_slots * kScaleBytes + (size_t)pl.q_slots * (block_bytes(bits) - kScaleBytes);
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kern::kRlThreads, dyn);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  // the barrier words live in the header slot: start them at zero
+  e = cudaMemsetAsync(buf, 0, kHeaderBytes, stream);
+  if (e != cudaSuccess) return e;
+  uint8_t* b = static_cast<uint8_t*>(buf);
+  kern::RelayoutPlan plan = pl;
+  void* args[] = {(void*)&b, (void*)&plan, (void*)&h};
+  return cudaLaunchCooperativeKernel(func, dim3((unsigned)sms), dim3(kern::kRlThreads), args, dyn, stream);
 }
 
 }  // namespace woq
