@@ -343,6 +343,9 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   const unsigned long long nb64 = (unsigned long long)p.T * (unsigned long long)p.G;
   if ((nb64 + 1) * (unsigned long long)(cfg.ctas + 1) >= (1ull << 32)) return WOQ_ERR_SHAPE;  // 32-bit partition math
   p.NB = (uint32_t)nb64;
+  p.div_c = FastDiv::make((uint32_t)cfg.ctas);
+  p.div_nb = FastDiv::make(p.NB);
+  p.div_g = FastDiv::make((uint32_t)p.G);
   p.stages = cfg.stages;
   p.prefetch_stages = cfg.prefetch_stages;
   p.act_stride = act_stride(K, cfg.consumer);

@@ -49,6 +49,7 @@
 #include <stdint.h>
 
 #include "woq_device.cuh"
+#include "woq_fastdiv.h"
 #include "woq_layout.h"
 #include "woq_prologue.cuh"
 #include "woq_scale_table.h"
@@ -67,6 +68,7 @@ struct GemvParams {
   unsigned long long* parts;  // [ctas][2][M][128] tagged partial sums of split tiles (tag << 32 | fp32 bits)
   int N, K, T, G;
   uint32_t NB;              // T * G blocks; (grid + 1) * NB < 2^32, so partition math stays 32-bit
+  FastDiv div_c, div_nb, div_g;  // division by the grid size, NB and G (multiply-high, no divide sequence)
   int stages;               // shared-memory ring stages
   int prefetch_stages;      // stages' worth of weights kept in flight into L2 beyond the ring
   int act_stride;           // bytes between activation rows of q in shared memory (K, or K + 16)
@@ -119,33 +121,40 @@ struct Fmt {
 };
 
 // first block of CTA c under an even split of NB blocks over C CTAs ((C + 1) * NB < 2^32)
-__device__ __forceinline__ uint32_t range_begin(uint32_t c, uint32_t NB, uint32_t C) { return c * NB / C; }
+__device__ __forceinline__ uint32_t range_begin(uint32_t c, uint32_t NB, const FastDiv& C) { return C.div(c * NB); }
 // CTA whose range holds block b
-__device__ __forceinline__ uint32_t cta_of_block(uint32_t b, uint32_t NB, uint32_t C) { return ((b + 1) * C - 1) / NB; }
+__device__ __forceinline__ uint32_t cta_of_block(uint32_t b, const FastDiv& NB, uint32_t C) { return NB.div((b + 1) * C - 1); }
 
 // Expected finish time, in blocks streamed, of CTA c's part of tile t, for a tile that
 // CTA c shares (its first or last tile) under the processing order of ItemOrder.
-__device__ __forceinline__ uint32_t part_finish(uint32_t c, uint32_t t, uint32_t NB, uint32_t C, uint32_t G) {
+__device__ __forceinline__ uint32_t part_finish(uint32_t c, uint32_t t, uint32_t NB, const FastDiv& C,
+                                                const FastDiv& G) {
   const uint32_t bb = range_begin(c, NB, C), be = range_begin(c + 1, NB, C);
-  const uint32_t ft = bb / G, lt = (be - 1) / G;
+  const uint32_t ft = G.div(bb), lt = G.div(be - 1);
   if (ft == lt) return be - bb;
-  const uint32_t a = (ft + 1) * G - bb;   // the start item, processed first
-  return t == ft ? a : a + (be - lt * G);  // the end item, processed second
+  const uint32_t a = (ft + 1) * G.d - bb;   // the start item, processed first
+  return t == ft ? a : a + (be - lt * G.d);  // the end item, processed second
 }
 
-// Whether this CTA combines split tile t: its part is expected to finish last (ties:
-// the lowest CTA).  Every CTA sharing the tile reaches the same answer.
-__device__ __forceinline__ bool is_combiner(uint32_t cta, uint32_t t, uint32_t NB, uint32_t C, uint32_t G) {
-  const uint32_t c_first = cta_of_block(t * G, NB, C), c_last = cta_of_block(t * G + G - 1, NB, C);
-  uint32_t comb = c_first, best = 0;
-  for (uint32_t c2 = c_first; c2 <= c_last; ++c2) {
-    const uint32_t f = part_finish(c2, t, NB, C, G);
-    if (c2 == c_first || f > best) {
-      best = f;
-      comb = c2;
+// The CTA that combines split tile t, shared by CTAs c_first .. c_last: the one whose part
+// is expected to finish last (ties: the lowest CTA).  Every CTA sharing the tile reaches
+// the same answer.  Warp-wide: lane k evaluates sharers c_first + k, c_first + k + 32, ...
+// and two warp reductions pick the largest finish time, then the lowest CTA holding it.
+__device__ __forceinline__ uint32_t combiner_of(uint32_t t, uint32_t c_first, uint32_t c_last, uint32_t NB,
+                                                const FastDiv& C, const FastDiv& G, int lane) {
+  uint32_t best_f = 0, best_c = 0xFFFFFFFFu;  // a sharer's part holds at least one block: f >= 1
+  for (uint32_t base = c_first; base <= c_last; base += 32) {  // warp-uniform
+    const uint32_t c2 = base + (uint32_t)lane;
+    if (c2 <= c_last) {
+      const uint32_t f = part_finish(c2, t, NB, C, G);
+      if (f > best_f) {  // a lane visits its sharers in increasing order: ties keep the lowest
+        best_f = f;
+        best_c = c2;
+      }
     }
   }
-  return comb == cta;
+  const uint32_t f_max = __reduce_max_sync(0xffffffffu, best_f);
+  return __reduce_min_sync(0xffffffffu, best_f == f_max ? best_c : 0xFFFFFFFFu);
 }
 
 // int4 / int6 lanes of word i of a 16-byte chunk: lo covers k0..k0+3, hi k0+4..k0+7
@@ -361,9 +370,10 @@ __device__ __forceinline__ void consume_half_block_mma(const uint8_t* __restrict
 struct ItemOrder {
   uint32_t b_begin, b_end, first_tile, last_tile;
   int G, n_items;
-  __device__ __forceinline__ ItemOrder(uint32_t bb, uint32_t be, int g) : b_begin(bb), b_end(be), G(g) {
-    first_tile = bb / (uint32_t)g;
-    last_tile = (be - 1) / (uint32_t)g;
+  __device__ __forceinline__ ItemOrder(uint32_t bb, uint32_t be, const FastDiv& g)
+      : b_begin(bb), b_end(be), G((int)g.d) {
+    first_tile = g.div(bb);
+    last_tile = g.div(be - 1);
     n_items = (int)(last_tile - first_tile + 1);
   }
   __device__ __forceinline__ void get(int i, uint32_t& t, int& ga, int& gb) const {
@@ -756,11 +766,11 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   const int lane = tid & 31;
   const uint32_t C = gridDim.x;
   const uint32_t cta = blockIdx.x;
-  const uint32_t b_begin = range_begin(cta, p.NB, C);
-  const uint32_t b_end = range_begin(cta + 1, p.NB, C);
+  const uint32_t b_begin = range_begin(cta, p.NB, p.div_c);
+  const uint32_t b_end = range_begin(cta + 1, p.NB, p.div_c);
   const int G = p.G;
   const int stages = p.stages;
-  const ItemOrder order(b_begin, b_end, G);
+  const ItemOrder order(b_begin, b_end, p.div_g);
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -838,6 +848,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   }
 
   // -------------------------------------------------------------------- consumers
+  if (tid == 0) WOQ_TRACE_EV(59);
   // roles in the split tiles (only the first two items can be split), worked out while the
   // previous grid may still be running
   // (per split item: whether this CTA combines it, the first and last CTA sharing the tile,
@@ -851,21 +862,22 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
     int ga, gb;
     order.get(0, t, ga, gb);
     if (!(ga == 0 && gb == G)) {
-      comb0 = is_combiner(cta, t, p.NB, C, (uint32_t)G);
-      cf0 = cta_of_block(t * G, p.NB, C);
-      cl0 = cta_of_block(t * G + G - 1, p.NB, C);
-      fp0 = range_begin(cf0, p.NB, C) < t * (uint32_t)G ? 1 : 0;
+      cf0 = cta_of_block(t * G, p.div_nb, C);
+      cl0 = cta_of_block(t * G + G - 1, p.div_nb, C);
+      comb0 = combiner_of(t, cf0, cl0, p.NB, p.div_c, p.div_g, lane) == cta;
+      fp0 = range_begin(cf0, p.NB, p.div_c) < t * (uint32_t)G ? 1 : 0;
     }
     if (order.n_items > 1) {
       order.get(1, t, ga, gb);
       if (!(ga == 0 && gb == G)) {
-        comb1 = is_combiner(cta, t, p.NB, C, (uint32_t)G);
-        cf1 = cta_of_block(t * G, p.NB, C);
-        cl1 = cta_of_block(t * G + G - 1, p.NB, C);
-        fp1 = range_begin(cf1, p.NB, C) < t * (uint32_t)G ? 1 : 0;
+        cf1 = cta_of_block(t * G, p.div_nb, C);
+        cl1 = cta_of_block(t * G + G - 1, p.div_nb, C);
+        comb1 = combiner_of(t, cf1, cl1, p.NB, p.div_c, p.div_g, lane) == cta;
+        fp1 = range_begin(cf1, p.NB, p.div_c) < t * (uint32_t)G ? 1 : 0;
       }
     }
   }
+  if (tid == 0) WOQ_TRACE_EV(58);
   // k ranges of the activations this CTA's blocks read: the start item's groups [ga, G) of
   // its first tile and, for a range that ends in a second tile, [0, gb) of that tile; with
   // whole tiles in between, everything
@@ -888,11 +900,11 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
       }
     }
   }
-  if constexpr (FUSED) {
-    // bring the row-scale tables into the constant cache while the previous grid runs
-    const uint32_t warm = kScaleSig[(tid * 4) & 127] ^ kRcpSig[(tid * 4) & 127];
-    asm volatile("" ::"r"(warm));
-  }
+  // bring the row-scale tables into the constant cache: issued here, waited for only after the
+  // activations have landed, so a CTA that starts late does not pass the grid wait later
+  uint32_t warm = 0;
+  if constexpr (FUSED) warm = kScaleSig[(tid * 4) & 127] ^ kRcpSig[(tid * 4) & 127];
+  if (tid == 0) WOQ_TRACE_EV(56);
   // activations (and y, the workspace) belong to the previous grid until it has completed
   dev::pdl_wait_prior_grids();
   uint4 hdr0 = make_uint4(0, 0, 0, 0), hdr1 = make_uint4(0, 0, 0, 0);
@@ -921,6 +933,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
     s_flags[1] = 1;
     atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
   }
+  asm volatile("" ::"r"(warm));
   if (tid == 0) {
     WOQ_TRACE_EV(4);
     // the packed header must describe this call's (bits, N, K)
