@@ -148,8 +148,10 @@ WOQ_API int woq_relayout_inplace(int bits, void* buf, size_t buf_bytes, int N, i
  * GPU's SMs; a 128-row tile that straddles CTAs is finished by one of them,
  * which sums the others' partial results (tagged words in the workspace) in a
  * fixed order.  The workspace (device, caller-owned) must be zero-filled once
- * before first use (woq_workspace_init); every successful launch leaves it zero
- * again (after a WOQ_DEVERR_TIMEOUT, zero-fill it again).  One workspace must
+ * before first use (woq_workspace_init); every successful launch leaves its
+ * synchronisation words zero again (after a WOQ_DEVERR_TIMEOUT, zero-fill it
+ * again).  Its last M * K * 2 bytes are scratch rows of the SwiGLU entries,
+ * overwritten by every such launch.  One workspace must
  * not be used by two launches that can run at the same time.  Its size depends
  * on the current device's SM count.
  * --------------------------------------------------------------------------- */

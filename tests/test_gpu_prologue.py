@@ -45,6 +45,7 @@ def _dev_bf16(a):
 def _gu_inputs(M, K, seed):
     gu = synthetic.gate_up_output(M, K, seed).numpy().copy()
     gu[0, :6] = [0.0, 100.0, -100.0, 50.0, -87.5, 88.8]  # exp underflow / overflow edges
+    gu[0, 6:10] = [-88.5, -88.7, -88.4, 87.3]  # e^-g with n = 128 in the scaling by 2^n, and near the top
     return gu
 
 
@@ -156,6 +157,35 @@ def test_fused_prologues_wide_m(M):
     out, ws = Guarded(M, N), Workspace(4, M, N, K)
     _run(woq.woq_w4a8_linear_swiglu_f32, wdev, torch.from_numpy(gu).to(DEV), N, K, out.y, ws.ws)
     assert tol_ok(out.numpy(), y_ref, S)[0]
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 17408, 5120), (4, 17408, 5120), (2, 5120, 1000)])
+def test_fused_swiglu_repeated_launches(M, K, N):
+    """The fused SwiGLU linear splits the SwiGLU over the grid (slices in the workspace
+    scratch rows, a grid-wide maximum): repeated launches on one workspace give identical
+    y, equal to twin + GEMV, and leave every word but the scratch rows zero.  The shapes
+    take the register route (M = 1) and the shared-memory route (M = 4) of the prologue."""
+    w, s = synthetic.weights(4, N, K, seed=K + M)
+    wdev = pack_host(4, to_numpy_u8(w), to_numpy_u16(s), N, K)
+    gu_dev = torch.from_numpy(_gu_inputs(M, K, seed=M + 5)).to(DEV)
+    nbytes = woq.woq_workspace_bytes(4, M, N, K)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    ys = []
+    for _ in range(3):
+        y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+        woq.woq_w4a8_linear_swiglu_f32(wdev, gu_dev, N, K, y, ws)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert woq.woq_read_status(ws) == 0
+    assert not ws[: nbytes - M * K * 2].cpu().numpy().any()
+    q = torch.empty((M, K), dtype=torch.int8, device=DEV)
+    a = torch.empty((M,), dtype=torch.float32, device=DEV)
+    woq.woq_swiglu_act_quant_int8(gu_dev, q, a)
+    y2 = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    woq.woq_w4a8_gemv(wdev, q, a, N, K, y2, ws)
+    torch.cuda.synchronize()
+    for y in ys:
+        assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
 
 
 def _sampled_rows(N, n_rand, seed):

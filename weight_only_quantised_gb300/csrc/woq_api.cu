@@ -145,11 +145,16 @@ LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
   return cfg;
 }
 
-WorkspaceLayout workspace_layout(int M, int N, int ctas) {
+// workspace: [0] status word, [64, 128) grid-barrier and row words of the SwiGLU prologue,
+// [256, ...) split-tile partial sums
+static constexpr size_t kSyncOffset = 64;
+
+WorkspaceLayout workspace_layout(int M, int N, int K, int ctas) {
   (void)N;
   WorkspaceLayout wl;
   wl.parts_offset = 256;
-  wl.total = wl.parts_offset + (size_t)ctas * 2 * (size_t)M * kTileRows * 8;
+  wl.h_offset = align_up(wl.parts_offset + (size_t)ctas * 2 * (size_t)M * kTileRows * 8, 256);
+  wl.total = wl.h_offset + (size_t)M * (size_t)K * 2;
   return wl;
 }
 
@@ -210,7 +215,7 @@ size_t woq_workspace_bytes(int bits, int M, int N, int K) {
   if (M == 0 || N == 0 || K == 0) return 256;  // empty shapes launch nothing
   const int c = max_ctas_for_workspace();
   if (c <= 0) return 0;
-  return workspace_layout(M, N, c).total;
+  return workspace_layout(M, N, K, c).total;
 }
 
 int woq_workspace_init(void* ws_dev, size_t ws_bytes, woq_stream_t stream) {
@@ -323,7 +328,7 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   if (wpacked_bytes < packed_bytes(bits, N, K)) return WOQ_ERR_LAYOUT;
   const LaunchConfig cfg = choose_config(bits, M, N, K, fused);
   if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
-  const WorkspaceLayout wl = workspace_layout(M, N, cfg.ctas);
+  const WorkspaceLayout wl = workspace_layout(M, N, K, cfg.ctas);
   if (ws_bytes < wl.total || cfg.ctas > max_ctas_for_workspace()) return WOQ_ERR_WORKSPACE;
   GemvParams p;
   p.w = static_cast<const uint8_t*>(wpacked);
@@ -336,6 +341,9 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<uint32_t*>(wsb);
   p.parts = reinterpret_cast<unsigned long long*>(wsb + wl.parts_offset);
+  p.sync = reinterpret_cast<uint32_t*>(wsb + kSyncOffset);
+  // the scratch rows are the last M K 2 bytes of the caller's workspace (16-byte aligned)
+  p.hbuf = reinterpret_cast<uint16_t*>(wsb + ((ws_bytes - (size_t)M * (size_t)K * 2) & ~(size_t)15));
   p.N = N;
   p.K = K;
   p.T = (N + kTileRows - 1) / kTileRows;
@@ -470,7 +478,7 @@ int woq_w4a8_linear_bf16_noalloc(const void* wpacked, size_t wpacked_bytes, cons
   if (K > 0) {
     const LaunchConfig cfg = choose_config(4, M, N, K, true);
     if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
-    need = workspace_layout(M, N, cfg.ctas).total;
+    need = workspace_layout(M, N, K, cfg.ctas).h_offset;  // the bf16 entry uses no scratch rows
   }
   if (need > kNoAllocScratchBytes) return WOQ_ERR_WORKSPACE;
   void* ws = nullptr;

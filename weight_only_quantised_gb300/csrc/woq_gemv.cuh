@@ -66,6 +66,8 @@ struct GemvParams {
   float* y;                 // fp32 [M][N]
   uint32_t* status;         // workspace status word
   unsigned long long* parts;  // [ctas][2][M][128] tagged partial sums of split tiles (tag << 32 | fp32 bits)
+  uint32_t* sync;           // workspace words of the grid-wide SwiGLU prologue (zero between launches)
+  uint16_t* hbuf;           // workspace scratch [M][K] bf16: the SwiGLU prologue's h, one slice per CTA
   int N, K, T, G;
   uint32_t NB;              // T * G blocks; (grid + 1) * NB < 2^32, so partition math stays 32-bit
   FastDiv div_c, div_nb, div_g;  // division by the grid size, NB and G (multiply-high, no divide sequence)
@@ -529,6 +531,19 @@ __device__ __forceinline__ void row_scales(const float (&lmax)[M], int tid, int 
   }
 }
 
+// Row scales from row amax values given in shared memory (the split SwiGLU prologue): the
+// same scale and reciprocal as row_scales, and the same consumer barrier.
+template <int M>
+__device__ __forceinline__ void given_row_scales(const float* amax_in, int tid, float* s_as, float (&sc)[M],
+                                                 float (&rc)[M]) {
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    scale_and_rcp(amax_in[m], sc[m], rc[m]);
+    if (tid == 0) s_as[m] = sc[m];
+  }
+}
+
 // Fast-route gate of a row: all ones when the fast route may decide (rc finite; an
 // all-zero row has rc = 0), else zero so that every vector of the row is redone.
 __device__ __forceinline__ uint32_t row_gate(float rc) { return rc <= 3.4028234e38f ? 0xFFFFFFFFu : 0u; }
@@ -536,7 +551,7 @@ __device__ __forceinline__ uint32_t row_gate(float rc) { return rc <= 3.4028234e
 template <int M>
 __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, int klo1, int khi1, int klo2, int khi2,
                                                   int tid, int lane, int warp, float* s_scratch, float* s_as,
-                                                  int launch_id) {
+                                                  int launch_id, const float* amax_in = nullptr) {
   constexpr int kVPR = kRegVecs / M;  // vectors per row held in registers
   constexpr int kStride = kConsumers * 8;  // values per vector round of all threads
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
@@ -550,18 +565,22 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
         const int k = 8 * tid + kStride * j;
         xv[m][j] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
       }
-    float lmax[M];
+    if (amax_in) {  // the row amax is given: only the barrier (every x value read before any q byte is written)
+      given_row_scales<M>(amax_in, tid, s_as, sc, rc);
+    } else {
+      float lmax[M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      uint32_t acc = 0;
+      for (int m = 0; m < M; ++m) {
+        uint32_t acc = 0;
 #pragma unroll
-      for (int j = 0; j < kVPR; ++j) {
-        if (kStride * j >= K) break;  // warp-uniform
-        acc = absmax8(acc, xv[m][j]);  // zeros beyond the row
+        for (int j = 0; j < kVPR; ++j) {
+          if (kStride * j >= K) break;  // warp-uniform
+          acc = absmax8(acc, xv[m][j]);  // zeros beyond the row
+        }
+        lmax[m] = dev::bf16x2_absmax_to_float(acc);
       }
-      lmax[m] = dev::bf16x2_absmax_to_float(acc);
+      row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
     }
-    row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
     if (tid == 0) WOQ_TRACE_EV2(5);
     dev::f32x2 rc2[M];
     uint32_t gate[M];
@@ -594,21 +613,26 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
     }
     return;
   }
-  // longer rows: amax pass, then rounds of 4 vectors per thread over each row
-  float lmax[M];
+  // longer rows: amax pass (unless given), then rounds of 4 vectors per thread over each row
+  if (amax_in) {
+    given_row_scales<M>(amax_in, tid, s_as, sc, rc);
+  } else {
+    float lmax[M];
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    uint32_t a[4] = {0u, 0u, 0u, 0u};
-    int k = 8 * tid;
-    for (; k + 3 * kStride < K; k += 4 * kStride) {
+    for (int m = 0; m < M; ++m) {
+      uint32_t a[4] = {0u, 0u, 0u, 0u};
+      int k = 8 * tid;
+      for (; k + 3 * kStride < K; k += 4 * kStride) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = absmax8(a[u], *reinterpret_cast<const uint4*>(xs + m * K + k + u * kStride));
+        for (int u = 0; u < 4; ++u)
+          a[u] = absmax8(a[u], *reinterpret_cast<const uint4*>(xs + m * K + k + u * kStride));
+      }
+      for (; k < K; k += kStride) a[0] = absmax8(a[0], *reinterpret_cast<const uint4*>(xs + m * K + k));
+      lmax[m] = dev::bf16x2_absmax_to_float(dev::bf16x2_absmax(dev::bf16x2_absmax(a[0], a[1]),
+                                                               dev::bf16x2_absmax(a[2], a[3])));
     }
-    for (; k < K; k += kStride) a[0] = absmax8(a[0], *reinterpret_cast<const uint4*>(xs + m * K + k));
-    lmax[m] = dev::bf16x2_absmax_to_float(dev::bf16x2_absmax(dev::bf16x2_absmax(a[0], a[1]),
-                                                             dev::bf16x2_absmax(a[2], a[3])));
+    row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);
   }
-  row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);
   if (tid == 0) WOQ_TRACE_EV2(5);
 #pragma unroll
   for (int m = 0; m < M; ++m) {
@@ -697,45 +721,158 @@ __device__ __forceinline__ void rmsnorm_prologue(uint8_t* act, int K, const uint
   dev::named_barrier_sync(kBarConsumers, kConsumers);
 }
 
-// SwiGLU of the fp32 gate+up rows in global memory into bf16 h at act [M][K].
+// SwiGLU of eight (gate, up) pairs at g, u -> eight bf16 h bits
+__device__ __forceinline__ uint4 swiglu8(const float* __restrict__ g, const float* __restrict__ u) {
+  const float4 g0 = __ldg(reinterpret_cast<const float4*>(g)), g1 = __ldg(reinterpret_cast<const float4*>(g + 4));
+  const float4 u0 = __ldg(reinterpret_cast<const float4*>(u)), u1 = __ldg(reinterpret_cast<const float4*>(u + 4));
+  const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = pro::swiglu_bf16(gg[2 * i], uu[2 * i]) | (pro::swiglu_bf16(gg[2 * i + 1], uu[2 * i + 1]) << 16);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Fused SwiGLU prologue, split over the grid.  h = SwiGLU(gate, up) of the fp32 [M][2K]
+// rows at gu (see woq_prologue.cuh).  The quantisation needs the largest |h| of each whole
+// row, and a CTA reads the k ranges of its own blocks, which many CTAs share.  So every CTA
+// forms h once for one C-th of each row, stores it (bf16) in the workspace scratch rows,
+// folds its largest |h| into the row words with red.max (h >= 0 as bits orders like the
+// values; the result does not depend on the order) and counts itself in with a release
+// reduction; once all C CTAs have (every CTA of this grid is resident, the wait is bounded)
+// it reads the row maxima and the h of its own ranges and quantises them like a bf16
+// activation.  sync (workspace, zero between launches): [0] arrivals, [2] departures
+// (CTAs that have read the maxima), [8 + m] row m's largest |h| bits; CTA 0 zeroes them at
+// the end of the launch (swiglu_sync_reset).
 template <int M>
-__device__ __forceinline__ void swiglu_prologue(uint8_t* act, int K, const float* __restrict__ gu, int tid) {
-  constexpr int kStride = kConsumers * 8;
-  uint16_t* hs = reinterpret_cast<uint16_t*>(act);
+__device__ __forceinline__ void swiglu_grid_max(uint32_t* sync, uint32_t C, const uint32_t (&acc)[M], int tid,
+                                                int lane, float* s_scratch, volatile int* s_ok, int launch_id) {
+  uint32_t* s_max = reinterpret_cast<uint32_t*>(s_scratch);  // [M] this CTA's largest |h| bits
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    const float* g = gu + (size_t)m * 2 * K;
-    const float* u = g + K;
-    for (int k0 = 8 * tid; k0 < K; k0 += 2 * kStride) {
-      float4 gv[2][2], uv[2][2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // two vectors' loads in flight before the arithmetic
-        const int k = k0 + h * kStride;
-        if (k < K) {
-          gv[h][0] = __ldg(reinterpret_cast<const float4*>(g + k));
-          gv[h][1] = __ldg(reinterpret_cast<const float4*>(g + k + 4));
-          uv[h][0] = __ldg(reinterpret_cast<const float4*>(u + k));
-          uv[h][1] = __ldg(reinterpret_cast<const float4*>(u + k + 4));
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int k = k0 + h * kStride;
-        if (k < K) {
-          const float gg[8] = {gv[h][0].x, gv[h][0].y, gv[h][0].z, gv[h][0].w,
-                               gv[h][1].x, gv[h][1].y, gv[h][1].z, gv[h][1].w};
-          const float uu[8] = {uv[h][0].x, uv[h][0].y, uv[h][0].z, uv[h][0].w,
-                               uv[h][1].x, uv[h][1].y, uv[h][1].z, uv[h][1].w};
-          uint32_t o[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            o[i] = pro::swiglu_bf16(gg[2 * i], uu[2 * i]) | (pro::swiglu_bf16(gg[2 * i + 1], uu[2 * i + 1]) << 16);
-          *reinterpret_cast<uint4*>(hs + m * K + k) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-    }
+    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(dev::bf16x2_absmax_to_float(acc[m])));
+    if (lane == 0 && wm) atomicMax(s_max + m, wm);
   }
   dev::named_barrier_sync(kBarConsumers, kConsumers);
+  if (tid == 0) {
+    WOQ_TRACE_EV2(61);
+    for (int m = 0; m < M; ++m)
+      if (s_max[m]) dev::red_max_relaxed_u32(sync + 8 + m, s_max[m]);
+    dev::red_add_release_u32(sync, 1u);  // ordered after the maxima
+    bool ok = true;
+    const uint64_t t0 = dev::global_timer_ns();
+    while (dev::ld_acquire_u32(sync) < C) {
+      if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) {
+        ok = false;
+        break;
+      }
+    }
+    for (int m = 0; m < M; ++m) s_scratch[8 + m] = __uint_as_float(ok ? dev::ld_acquire_u32(sync + 8 + m) : 0u);
+    if (ok) dev::red_add_release_u32(sync + 2, 1u);  // after the reads above
+    *s_ok = ok ? 1 : 0;
+    WOQ_TRACE_EV2(62);
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+}
+
+// Returns 0 if the wait ran out, 1 if q is formed (register route), 2 if h is in the
+// activation area and the caller quantises it with the row maxima at s_scratch + 8.
+template <int M>
+__device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs, const float* __restrict__ gu,
+                                                     uint32_t* sync, uint16_t* hbuf, uint32_t cta, uint32_t C,
+                                                     int klo1, int khi1, int klo2, int khi2, int tid, int lane,
+                                                     int warp, float* s_scratch, float* s_as, volatile int* s_ok,
+                                                     int launch_id) {
+  constexpr int kStride = kConsumers * 8;
+  constexpr int kHV = M <= 4 ? 4 / M : 1;  // vectors per row and range kept in registers
+  uint32_t* s_max = reinterpret_cast<uint32_t*>(s_scratch);
+  if (tid < M) s_max[tid] = 0u;
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+  if (tid == 0) WOQ_TRACE_EV2(60);
+  // this CTA's slice of every row, in 8-value vectors: h once, into the scratch rows
+  const int nv = K / 8;
+  const int v_lo = (int)((unsigned long long)cta * (unsigned)nv / C);
+  const int v_hi = (int)((unsigned long long)(cta + 1) * (unsigned)nv / C);
+  uint32_t acc[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) acc[m] = 0u;
+  for (int v = v_lo + tid; v < v_hi; v += kConsumers) {
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const uint4 h = swiglu8(gu + (size_t)m * 2 * K + 8 * v, gu + (size_t)m * 2 * K + K + 8 * v);
+      *reinterpret_cast<uint4*>(hbuf + (size_t)m * K + 8 * v) = h;
+      acc[m] = absmax8(acc[m], h);
+    }
+  }
+  swiglu_grid_max<M>(sync, C, acc, tid, lane, s_scratch, s_ok, launch_id);  // also publishes the slices
+  if (!*s_ok) return 0;
+  // h of the k ranges this CTA's blocks read, written by the CTAs that own those slices
+  // (read through L2: this SM's L1 may hold an older launch's lines)
+  if (khi1 - klo1 <= kHV * kStride && khi2 - klo2 <= kHV * kStride) {  // register route (CTA-uniform)
+    uint4 hv[2][kHV][M];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int j = 0; j < kHV; ++j) {
+        const int k = (r == 0 ? klo1 : klo2) + 8 * tid + j * kStride;
+        if (k < (r == 0 ? khi1 : khi2)) {
+#pragma unroll
+          for (int m = 0; m < M; ++m) hv[r][j][m] = __ldcg(reinterpret_cast<const uint4*>(hbuf + (size_t)m * K + k));
+        }
+      }
+    float sc[M];
+    dev::f32x2 rc2[M];
+    uint32_t gate[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      float rc;
+      scale_and_rcp(s_scratch[8 + m], sc[m], rc);
+      rc2[m] = dev::f2_splat(rc);
+      gate[m] = row_gate(rc);
+    }
+    if (tid < M) s_as[tid] = sc[tid];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int j = 0; j < kHV; ++j) {
+        const int k = (r == 0 ? klo1 : klo2) + 8 * tid + j * kStride;
+        if (k < (r == 0 ? khi1 : khi2)) {
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            uint32_t gm = gate[m];
+            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(hv[r][j][m], rc2[m], gm);
+            if (!(gm >> 31)) *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_exact(hv[r][j][m], sc[m]);
+          }
+        }
+      }
+    return 1;
+  }
+  // shared-memory route: h (bf16) of the ranges into the activation area
+  uint16_t* hs = reinterpret_cast<uint16_t*>(act);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int lo = r == 0 ? klo1 : klo2, hi = r == 0 ? khi1 : khi2;
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+      for (int k = lo + 8 * tid; k < hi; k += kStride)
+        *reinterpret_cast<uint4*>(hs + m * K + k) = __ldcg(reinterpret_cast<const uint4*>(hbuf + (size_t)m * K + k));
+  }
+  return 2;
+}
+
+// End of a launch with the split SwiGLU prologue: CTA 0 waits (bounded) until every CTA
+// has read the row maxima, then zeroes the words for the next launch.  false on timeout.
+template <int M>
+__device__ __forceinline__ bool swiglu_sync_reset(uint32_t* sync, uint32_t C) {
+  const uint64_t t0 = dev::global_timer_ns();
+  while (dev::ld_acquire_u32(sync + 2) < C)
+    if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) return false;
+  sync[0] = 0u;
+  sync[2] = 0u;
+#pragma unroll
+  for (int m = 0; m < M; ++m) sync[8 + m] = 0u;
+  return true;
 }
 
 // Consumer of a kernel instance: every consumer warp on dp4a, or every one on the f16
@@ -753,7 +890,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);          // [8]
   uint64_t* empty = full + 8;                                  // [8]
   uint64_t* actbar = full + 16;                                // activations landed
-  volatile int* s_flags = reinterpret_cast<volatile int*>(smem + 136);  // [0] ticket-last, [1] abort, [2] header-ok
+  volatile int* s_flags = reinterpret_cast<volatile int*>(smem + 136);  // [0] ticket-last, [1] abort, [2] header-ok, [3] prologue barrier ok
   float* s_as = reinterpret_cast<float*>(smem + 160);          // [M] activation scales
   float* s_scratch = reinterpret_cast<float*>(smem + 192);     // [8 rows][8 warps] amax partials, to byte 448
   unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(smem + 448);  // [8] RMSNorm sums of squares
@@ -946,8 +1083,22 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   }
   if constexpr (PRO == kProRms)
     rmsnorm_prologue<M>(act, p.K, p.gamma, p.eps, tid, lane, reinterpret_cast<uint32_t*>(s_scratch), s_sum);
-  if constexpr (PRO == kProSwiglu) swiglu_prologue<M>(act, p.K, static_cast<const float*>(p.x), tid);
-  if constexpr (FUSED) {
+  if constexpr (PRO == kProSwiglu) {
+    const int route = swiglu_split_prologue<M>(act, p.K, p.act_stride, static_cast<const float*>(p.x), p.sync,
+                                               p.hbuf, cta, C, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch,
+                                               s_as, s_flags + 3, p.launch_id);
+    if (route == 2)
+      quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
+                           p.launch_id, s_scratch + 8);
+    if (tid == 0) WOQ_TRACE_EV(63);
+    if (route == 0) {
+      aborted = true;
+      if (tid == 0) {
+        s_flags[1] = 1;
+        atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
+      }
+    }
+  } else if constexpr (FUSED) {
     quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
                          p.launch_id);
   } else {
@@ -1134,6 +1285,10 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
         }
       }
     }
+  }
+  if constexpr (PRO == kProSwiglu) {
+    if (cta == 0 && tid == 0 && s_flags[3] && !swiglu_sync_reset<M>(p.sync, C))
+      atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
   }
   if (tid == 0) WOQ_TRACE_EV(8);
 }

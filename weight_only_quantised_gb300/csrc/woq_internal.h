@@ -22,7 +22,8 @@ struct LaunchConfig {
 
 // Workspace layout: [status word + pad: 256 B][tagged partial sums: ctas x 2 x M x 128 x 8 B]
 struct WorkspaceLayout {
-  size_t parts_offset;
+  size_t parts_offset;  // split-tile partial sums
+  size_t h_offset;      // SwiGLU prologue scratch rows (bf16 [M][K]); no zeroing needed
   size_t total;
 };
 
@@ -36,7 +37,7 @@ int max_dynamic_smem();               // opt-in shared memory per block of the c
 int choose_consumer(int bits, int M);  // kern::Consumer the launch table picks for (bits, M)
 int smem_bytes_for(int bits, int M, int K, bool fused, int stages);
 LaunchConfig choose_config(int bits, int M, int N, int K, bool fused);
-WorkspaceLayout workspace_layout(int M, int N, int ctas);
+WorkspaceLayout workspace_layout(int M, int N, int K, int ctas);
 
 // Kernel launchers (woq_gemv.cu); return a cudaError_t.
 cudaError_t launch_gemv(int bits, bool fused, int M, int N, int K, const void* wpacked, const void* x_bf16,

@@ -15,7 +15,7 @@
 //     up u = columns K .. 2K-1: h = bf16(RN(RN(g sg) u)), sg = RN(1 / RN(1 + e)),
 //     e = e^-g by Cody and Waite's method: n = rint(RN(a log2 e)), r = a - n ln2 with
 //     ln2 split into a 10-bit head and a tail (two fused multiply-adds), the degree-7
-//     Taylor polynomial of e^r by Horner's rule in fused multiply-adds, scaled by 2^n;
+//     Taylor polynomial of e^r by Horner's rule in fused multiply-adds, times 2^n (one rounding);
 //     a >= 88.72 gives +inf, a <= -87 gives 0.
 #pragma once
 
@@ -42,7 +42,11 @@ __device__ __forceinline__ float exp_cw(float a) {
   p = __fmaf_rn(p, r, 0.5f);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  return ldexpf(p, (int)n);
+  // p 2^n, rounded once: n is in [-126, 128] here, so 2^n is a normal float but for n = 128,
+  // which takes two exact steps (p 2^127 is exact; doubling it rounds once)
+  const int ni = (int)n;
+  if (ni > 127) return __fmul_rn(__fmul_rn(p, 0x1p127f), 2.0f);
+  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
 }
 
 __device__ __forceinline__ uint32_t f32_to_bf16_bits(float v) {

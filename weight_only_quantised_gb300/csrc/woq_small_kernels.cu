@@ -307,29 +307,21 @@ struct RelayoutPlan {
   int scale_slots;      // blocks whose scales a CTA stages for the whole run
 };
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // Grid barrier on words[0] (arrivals) and words[1] (generation); bounded.
 __device__ bool rl_grid_barrier(uint32_t* words, int* s_ok) {
   __syncthreads();
   if (threadIdx.x == 0) {
     bool ok = true;
-    const uint32_t gen = ld_acquire_u32(words + 1);
+    const uint32_t gen = dev::ld_acquire_u32(words + 1);
     __threadfence();
     if (atomicAdd(words, 1u) == gridDim.x - 1) {
       atomicExch(words, 0u);
       __threadfence();
-      st_release_u32(words + 1, gen + 1);
+      dev::st_release_u32(words + 1, gen + 1);
     } else {
       const uint64_t t0 = dev::global_timer_ns();
-      while (ld_acquire_u32(words + 1) == gen) {
+      while (dev::ld_acquire_u32(words + 1) == gen) {
         if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) {
           ok = false;
           break;
@@ -408,7 +400,7 @@ __global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, Rela
   if (tid == 0) {  // CTA 0 waits for every CTA, so nobody still reads the barrier words
     bool ok = true;
     const uint64_t t0 = dev::global_timer_ns();
-    while (ld_acquire_u32(words + 3) != (uint32_t)C) {
+    while (dev::ld_acquire_u32(words + 3) != (uint32_t)C) {
       if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) {
         ok = false;
         break;
