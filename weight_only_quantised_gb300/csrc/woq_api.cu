@@ -55,14 +55,14 @@ int max_dynamic_smem() {
   return v;
 }
 
-// [barriers, flags, scratch: 512][reduction buffer][activations][ring]
+// [barriers, flags, scratch: 1024][reduction buffer][activations][ring]
 // activations: bf16 x quantised in place (fused, 2 M K bytes) or int8 q (M rows); kernels
 // with tensor-core warps read q rows padded to K + 16 bytes (conflict-free fragment loads).
 // In the fused entry q needs only the first M (K or K + 16) bytes once the prologue is
 // done, and the reduction buffer is first written after it, so when the bf16 tail is
-// large enough the reduction buffer lives there: [512][activations (q + reduction)][ring].
+// large enough the reduction buffer lives there: [1024][activations (q + reduction)][ring].
 static int red_bytes(int M) { return kStageBlocks * M * kTileRows * 4; }
-static constexpr int kMiscBytes = 512;
+static constexpr int kMiscBytes = 1024;  // barriers, flags, row scales and scratch (see the kernel)
 static int act_stride(int K, int cons) { return cons != kern::kDp4a ? K + 16 : K; }
 static int act_bytes(int M, int K, bool fused, int cons) { return fused ? 2 * M * K : M * act_stride(K, cons); }
 static int q_end(int M, int K, int cons) { return (int)align_up((size_t)M * act_stride(K, cons), 16); }

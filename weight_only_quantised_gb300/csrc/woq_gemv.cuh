@@ -721,6 +721,97 @@ __device__ __forceinline__ void rmsnorm_prologue(uint8_t* act, int K, const uint
   dev::named_barrier_sync(kBarConsumers, kConsumers);
 }
 
+// RMSNorm and quantisation of rows held in registers (K <= kRmsRegVecs * 2048, M <= 4):
+// the same steps and arithmetic as rmsnorm_prologue followed by quantise_prologue (row
+// exponent, exact integer sum of squares, r, h = bf16(RN(RN(x r) gamma)), the row's largest
+// |h|, q for the CTA's k ranges), with x read from shared memory once, gamma already in
+// registers (loaded before the grid wait: it is a weight) and h never written back.
+// s_bits: [0, M) row max |x| bits, [8, 8 + M) row max |h| bits, zero on entry; s_part:
+// [M][8 warps] sums of squares, written before they are read.
+constexpr int kRmsRegVecs = 3;
+template <int M>
+__device__ __forceinline__ void rmsnorm_quantise_regs(uint8_t* act, int K, int qs, const uint4 (&gv)[kRmsRegVecs],
+                                                      float eps, int klo1, int khi1, int klo2, int khi2, int tid,
+                                                      int lane, uint32_t* s_bits, unsigned long long* s_part,
+                                                      float* s_as, int launch_id) {
+  constexpr int kStride = kConsumers * 8;
+  const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
+  if (tid == 0) WOQ_TRACE_EV2(60);
+  uint4 v[M][kRmsRegVecs];
+#pragma unroll
+  for (int m = 0; m < M; ++m)
+#pragma unroll
+    for (int j = 0; j < kRmsRegVecs; ++j) {
+      const int k = 8 * tid + kStride * j;
+      v[m][j] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int j = 0; j < kRmsRegVecs; ++j) acc = absmax8(acc, v[m][j]);
+    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(dev::bf16x2_absmax_to_float(acc)));
+    if (lane == 0 && wm) atomicMax(s_bits + m, wm);
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);  // also: every x value read before any q byte is written
+  if (tid == 0) WOQ_TRACE_EV2(61);
+  int C[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    C[m] = pro::rms_row_exponent(s_bits[m]);
+    unsigned long long part = 0;
+    if (C[m] != -1000) {
+#pragma unroll
+      for (int j = 0; j < kRmsRegVecs; ++j) {  // zero vectors beyond the row add nothing
+        const uint32_t w[4] = {v[m][j].x, v[m][j].y, v[m][j].z, v[m][j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) part += pro::rms_term(w[i] & 0xFFFFu, C[m]) + pro::rms_term(w[i] >> 16, C[m]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) s_part[m * 8 + (tid >> 5)] = part;  // one slot per warp: no atomics
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+  if (tid == 0) WOQ_TRACE_EV2(62);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    unsigned long long S = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) S += s_part[m * 8 + w];  // integer: any order gives the same sum
+    const float r = C[m] == -1000 ? 0.0f : pro::rms_rcp(S, C[m], K, eps);
+    uint32_t acc = 0;
+#pragma unroll
+    for (int j = 0; j < kRmsRegVecs; ++j) {
+      if (8 * tid + kStride * j < K) {
+        v[m][j] = pro::rms_h8(v[m][j], gv[j], r);
+        acc = absmax8(acc, v[m][j]);
+      }
+    }
+    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(dev::bf16x2_absmax_to_float(acc)));
+    if (lane == 0 && wm) atomicMax(s_bits + 8 + m, wm);
+  }
+  dev::named_barrier_sync(kBarConsumers, kConsumers);
+  if (tid == 0) WOQ_TRACE_EV2(63);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    float sc, rc;
+    scale_and_rcp(__uint_as_float(s_bits[8 + m]), sc, rc);
+    if (tid == 0) s_as[m] = sc;
+    const dev::f32x2 rc2 = dev::f2_splat(rc);
+    const uint32_t gate = row_gate(rc);
+#pragma unroll
+    for (int j = 0; j < kRmsRegVecs; ++j) {
+      const int k = 8 * tid + kStride * j;
+      if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {
+        uint32_t g = gate;
+        *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(v[m][j], rc2, g);
+        if (!(g >> 31)) *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_exact(v[m][j], sc);  // rare
+      }
+    }
+  }
+}
+
 // SwiGLU of eight (gate, up) pairs at g, u -> eight bf16 h bits
 __device__ __forceinline__ uint4 swiglu8(const float* __restrict__ g, const float* __restrict__ u) {
   const float4 g0 = __ldg(reinterpret_cast<const float4*>(g)), g1 = __ldg(reinterpret_cast<const float4*>(g + 4));
@@ -894,6 +985,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   float* s_as = reinterpret_cast<float*>(smem + 160);          // [M] activation scales
   float* s_scratch = reinterpret_cast<float*>(smem + 192);     // [8 rows][8 warps] amax partials, to byte 448
   unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(smem + 448);  // [8] RMSNorm sums of squares
+  unsigned long long* s_part = reinterpret_cast<unsigned long long*>(smem + 512);  // [8 rows][8 warps] of them
   uint8_t* act = smem + p.act_offset;                          // bf16 x, quantised in place (fused) or int8 q
   float* red = reinterpret_cast<float*>(smem + p.red_offset);  // [4 blocks][M][128 rows]
   uint8_t* ring = smem + p.ring_offset;
@@ -921,10 +1013,8 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
     dev::fence_mbar_init();
   }
   if constexpr (PRO == kProRms) {
-    if (tid < 8) {
-      reinterpret_cast<uint32_t*>(s_scratch)[tid] = 0u;
-      s_sum[tid] = 0ull;
-    }
+    if (tid < 16) reinterpret_cast<uint32_t*>(s_scratch)[tid] = 0u;
+    if (tid < 8) s_sum[tid] = 0ull;
   }
   __syncthreads();
   if (tid == 0) WOQ_TRACE_EV(0);
@@ -1041,10 +1131,27 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
   // activations have landed, so a CTA that starts late does not pass the grid wait later
   uint32_t warm = 0;
   if constexpr (FUSED) warm = kScaleSig[(tid * 4) & 127] ^ kRcpSig[(tid * 4) & 127];
+  // RMSNorm rows that fit registers: gamma (a weight) is loaded before the grid wait
+  constexpr bool kRmsRegPath = PRO == kProRms && M <= 4;
+  const bool rms_regs = kRmsRegPath && p.K <= kConsumers * 8 * kRmsRegVecs;
+  uint4 gv[kRmsRegVecs];
+  if constexpr (kRmsRegPath) {
+#pragma unroll
+    for (int j = 0; j < kRmsRegVecs; ++j) {
+      const int k = 8 * tid + kConsumers * 8 * j;
+      gv[j] = rms_regs && k < p.K ? __ldg(reinterpret_cast<const uint4*>(p.gamma + k)) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  // the packed header (weights: not written by the previous grid) is fetched before the wait;
+  // the ring never reads it, so it would cost a DRAM round trip on the critical path
+  uint4 hdr0 = make_uint4(0, 0, 0, 0), hdr1 = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    hdr0 = __ldg(reinterpret_cast<const uint4*>(p.w));
+    hdr1 = __ldg(reinterpret_cast<const uint4*>(p.w + 16));
+  }
   if (tid == 0) WOQ_TRACE_EV(56);
   // activations (and y, the workspace) belong to the previous grid until it has completed
   dev::pdl_wait_prior_grids();
-  uint4 hdr0 = make_uint4(0, 0, 0, 0), hdr1 = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     WOQ_TRACE_EV(3);
     const uint32_t act_bytes = (uint32_t)(FUSED ? 2 * M * p.K : M * p.K);
@@ -1058,8 +1165,6 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
       for (int m = 0; m < M; ++m)
         dev::bulk_copy_g2s(act + m * p.act_stride, p.q + (size_t)m * p.K, (uint32_t)p.K, actbar);
     }
-    hdr0 = *reinterpret_cast<const uint4*>(p.w);
-    hdr1 = *reinterpret_cast<const uint4*>(p.w + 16);
   }
   float ascale_in = 0.0f;
   if (!FUSED && tid < M) ascale_in = p.ascale[tid];
@@ -1081,8 +1186,16 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
       atomicOr(p.status, 0x1u /* WOQ_DEVERR_HEADER */);
     }
   }
+  bool quantised = false;
+  if constexpr (kRmsRegPath) {
+    if (rms_regs) {
+      rmsnorm_quantise_regs<M>(act, p.K, p.act_stride, gv, p.eps, klo1, khi1, klo2, khi2, tid, lane,
+                               reinterpret_cast<uint32_t*>(s_scratch), s_part, s_as, p.launch_id);
+      quantised = true;
+    }
+  }
   if constexpr (PRO == kProRms)
-    rmsnorm_prologue<M>(act, p.K, p.gamma, p.eps, tid, lane, reinterpret_cast<uint32_t*>(s_scratch), s_sum);
+    if (!quantised) rmsnorm_prologue<M>(act, p.K, p.gamma, p.eps, tid, lane, reinterpret_cast<uint32_t*>(s_scratch), s_sum);
   if constexpr (PRO == kProSwiglu) {
     const int route = swiglu_split_prologue<M>(act, p.K, p.act_stride, static_cast<const float*>(p.x), p.sync,
                                                p.hbuf, cta, C, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch,
@@ -1099,8 +1212,9 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
       }
     }
   } else if constexpr (FUSED) {
-    quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
-                         p.launch_id);
+    if (!quantised)
+      quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
+                           p.launch_id);
   } else {
     if (tid < M) s_as[tid] = ascale_in;
   }

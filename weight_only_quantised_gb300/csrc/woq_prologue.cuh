@@ -66,15 +66,17 @@ __device__ __forceinline__ int bf16_exp_c(uint32_t b16) {
   return ef ? (int)ef - 134 : ((b16 & 0x7Fu) ? -133 : -1000);
 }
 
-// a^2 2^(2c - 2C + 30) rounded down, for one bf16 value against the row exponent C
+// a^2 2^(2c - 2C + 30) rounded down, for one bf16 value against the row exponent C (c <= C,
+// so the shift is at most 30: a^2 < 2^16 times 2^sh is one 32 x 32 -> 64-bit product, and a
+// negative shift leaves a 32-bit value, zero once it reaches 16)
 __device__ __forceinline__ unsigned long long rms_term(uint32_t b16, int C) {
   const uint32_t ef = (b16 >> 7) & 0xFFu, f = b16 & 0x7Fu;
   const uint32_t a = ef ? 128u + f : f;
   const int c = ef ? (int)ef - 134 : -133;
-  const unsigned long long a2 = (unsigned long long)(a * a);
+  const uint32_t a2 = a * a;
   const int sh = 2 * c - 2 * C + 30;
-  if (sh >= 0) return a2 << sh;
-  return sh > -64 ? a2 >> (-sh) : 0ull;
+  if (sh >= 0) return (unsigned long long)a2 * (1u << sh);
+  return -sh < 16 ? (unsigned long long)(a2 >> (-sh)) : 0ull;
 }
 
 // r = RN(1 / RN(sqrt(RN(ms + eps)))) from the row's integer sum of squares
