@@ -197,19 +197,36 @@ __host__ __device__ inline size_t canonical_row_bytes(int bits, int K) {
 // The packed words of one chunk (one row, one 32-k quarter) from its canonical bytes:
 // 16 bytes of int4 (two per byte, low nibble = even k) or 24 bytes of int6 (four per
 // three bytes).  lo: the int4 / low-nibble words, hi: the int6 high-bit words.
+// The canonical bytes of one chunk (32 weights of one row): 16 (int4) or 24 (int6) bytes.
+struct RawChunk {
+  uint32_t w[6];
+};
 template <int BITS>
-__device__ __forceinline__ void pack_chunk(const uint8_t* __restrict__ src, uint32_t (&lo)[4], uint32_t (&hi)[2]) {
-  uint8_t code[32];
+__device__ __forceinline__ RawChunk load_chunk(const uint8_t* __restrict__ src) {
+  RawChunk r = {{0u, 0u, 0u, 0u, 0u, 0u}};
   if constexpr (BITS == 4) {
     const uint4 v = *reinterpret_cast<const uint4*>(src);
-    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int kk = 0; kk < 32; ++kk) code[kk] = (uint8_t)((vw[kk >> 3] >> (4 * (kk & 7))) & 0xF);
+    r.w[0] = v.x, r.w[1] = v.y, r.w[2] = v.z, r.w[3] = v.w;
   } else {
     const uint2 a = *reinterpret_cast<const uint2*>(src);
     const uint2 b = *reinterpret_cast<const uint2*>(src + 8);
     const uint2 cc = *reinterpret_cast<const uint2*>(src + 16);
-    const uint32_t bw[6] = {a.x, a.y, b.x, b.y, cc.x, cc.y};
+    r.w[0] = a.x, r.w[1] = a.y, r.w[2] = b.x, r.w[3] = b.y, r.w[4] = cc.x, r.w[5] = cc.y;
+  }
+  return r;
+}
+
+// A chunk's canonical bytes -> its packed words (lo: the int4 region's 16 bytes; hi: the
+// int6 top-bit plane's 8 bytes).
+template <int BITS>
+__device__ __forceinline__ void convert_chunk(const RawChunk& raw, uint32_t (&lo)[4], uint32_t (&hi)[2]) {
+  uint8_t code[32];
+  if constexpr (BITS == 4) {
+    const uint32_t* vw = raw.w;
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) code[kk] = (uint8_t)((vw[kk >> 3] >> (4 * (kk & 7))) & 0xF);
+  } else {
+    const uint32_t* bw = raw.w;
 #pragma unroll
     for (int quad = 0; quad < 8; ++quad) {
       uint32_t word = 0;
@@ -243,6 +260,11 @@ __device__ __forceinline__ void pack_chunk(const uint8_t* __restrict__ src, uint
         hi[h] |= ((uint32_t)((cb >> 4) & 3) << (2 * (2 * e + 1))) << (8 * b);
       }
   }
+}
+
+template <int BITS>
+__device__ __forceinline__ void pack_chunk(const uint8_t* __restrict__ src, uint32_t (&lo)[4], uint32_t (&hi)[2]) {
+  convert_chunk<BITS>(load_chunk<BITS>(src), lo, hi);
 }
 template <int BITS>
 __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ scales, int N, int K, int T,
@@ -290,7 +312,8 @@ __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __res
 // below the canonical bytes of any lower tile (G BB >= 128 row bytes), so the tiles are
 // rewritten in batches of whole tiles from the top down: every CTA first copies all the
 // scales it will write into shared memory (the top tiles overwrite the scale region),
-// then per batch gathers its blocks' canonical chunks, converted to the packed order,
+// then per batch gathers its blocks' canonical chunks (a contiguous run of the batch's
+// blocks, so rows are read in long segments), converted to the packed order,
 // into shared memory, meets the other CTAs at a grid barrier (every read of the batch is
 // done) and writes them out.  The 256-byte header slot holds the barrier words (0: arrivals,
 // 1: generation, 2: failure, 3: departures) until CTA 0, once every CTA has counted its
@@ -355,7 +378,8 @@ __global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, Rela
   for (int thi = pl.T; thi > 0; thi -= pl.tiles_per_batch) {
     const int tlo = thi > pl.tiles_per_batch ? thi - pl.tiles_per_batch : 0;
     const int nb = (thi - tlo) * pl.G;
-    for (int i = cta; i < nb; i += C, ++slot) {
+    const int i_lo = (int)((long long)cta * nb / C), i_hi = (int)((long long)(cta + 1) * nb / C);
+    for (int i = i_lo; i < i_hi; ++i, ++slot) {
       const int b = tlo * pl.G + i, t = b / pl.G, g = b % pl.G;
       for (int r = tid; r < kTileRows; r += kRlThreads) {
         const int n = t * kTileRows + r;
@@ -366,24 +390,41 @@ __global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, Rela
   if (!rl_grid_barrier(words, &s_ok)) return;
 
   slot = 0;
-  const int l = tid & 31, j = (tid >> 5) & 3, c4 = tid >> 7;  // this thread's chunk of every block
+  // this thread's chunk of every block: four consecutive lanes take the four 32-k quarters of
+  // one row, so a warp reads eight rows' contiguous 64 (int4) or 96 (int6) bytes of the group
+  const int c4 = tid & 3, r = tid >> 2, j = r >> 5, l = r & 31;
   for (int thi = pl.T; thi > 0; thi -= pl.tiles_per_batch) {
     const int tlo = thi > pl.tiles_per_batch ? thi - pl.tiles_per_batch : 0;
     const int nb = (thi - tlo) * pl.G;
-    int k = 0;
-    for (int i = cta; i < nb; i += C, ++k) {  // gather, converted to the packed order
-      const int b = tlo * pl.G + i, t = b / pl.G, g = b % pl.G;
-      const int n = t * kTileRows + 32 * j + l;
-      uint32_t lo[4] = {0u, 0u, 0u, 0u};
-      uint32_t hi[2] = {0u, 0u};
-      if (n < pl.N) pack_chunk<BITS>(canon_q + (size_t)n * R + (size_t)(g * kGroup + 32 * c4) * BITS / 8, lo, hi);
-      uint8_t* sb = s_q + (size_t)k * QB - kScaleBytes;  // chunk offsets count from the block start
-      *reinterpret_cast<uint4*>(sb + w4_chunk_offset(c4, j, l)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      if constexpr (BITS == 6) *reinterpret_cast<uint2*>(sb + hi_chunk_offset(c4, j, l)) = make_uint2(hi[0], hi[1]);
+    const int i_lo = (int)((long long)cta * nb / C), i_hi = (int)((long long)(cta + 1) * nb / C);
+    // gather, converted to the packed order; kUnroll blocks' loads in flight before converting
+    constexpr int kUnroll = 4;
+    for (int i0 = i_lo, k0 = 0; i0 < i_hi; i0 += kUnroll, k0 += kUnroll) {
+      RawChunk raw[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = i0 + u;
+        raw[u] = RawChunk{{0u, 0u, 0u, 0u, 0u, 0u}};
+        if (i < i_hi) {
+          const int b = tlo * pl.G + i, t = b / pl.G, g = b % pl.G;
+          const int n = t * kTileRows + 32 * j + l;
+          if (n < pl.N) raw[u] = load_chunk<BITS>(canon_q + (size_t)n * R + (size_t)(g * kGroup + 32 * c4) * BITS / 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (i0 + u >= i_hi) break;
+        uint32_t lo[4], hi[2];
+        convert_chunk<BITS>(raw[u], lo, hi);
+        uint8_t* sb = s_q + (size_t)(k0 + u) * QB - kScaleBytes;  // chunk offsets count from the block start
+        *reinterpret_cast<uint4*>(sb + w4_chunk_offset(c4, j, l)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if constexpr (BITS == 6)
+          *reinterpret_cast<uint2*>(sb + hi_chunk_offset(c4, j, l)) = make_uint2(hi[0], hi[1]);
+      }
     }
     if (!rl_grid_barrier(words, &s_ok)) return;  // every canonical byte of the batch has been read
-    k = 0;
-    for (int i = cta; i < nb; i += C, ++k, ++slot) {
+    int k = 0;
+    for (int i = i_lo; i < i_hi; ++i, ++k, ++slot) {
       uint8_t* out = buf + kHeaderBytes + (size_t)(tlo * pl.G + i) * BB;
       for (int e = tid; e < kScaleBytes / 16; e += kRlThreads)
         reinterpret_cast<uint4*>(out)[e] = reinterpret_cast<const uint4*>(s_scales + (size_t)slot * kTileRows)[e];
