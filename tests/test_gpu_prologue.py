@@ -86,8 +86,10 @@ def _run(fn, *args):
 
 @pytest.mark.parametrize("bits,path", BITS_PATHS)
 @pytest.mark.parametrize("M", [1, 3, 4])
-@pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (2048, 5120)])
+@pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (2048, 5120), (700, 6144), (700, 6272)])
 def test_fused_rmsnorm_linear(bits, path, M, N, K):
+    """K = 6144 is the largest row the fused RMSNorm keeps in registers (M <= 4); 6272 takes
+    the shared-memory passes."""
     woq.woq_tune_path(path)
     w, s = synthetic.weights(bits, N, K, seed=3 * N + K + bits)
     wn, sn = to_numpy_u8(w), to_numpy_u16(s)
