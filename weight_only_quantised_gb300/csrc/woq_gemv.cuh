@@ -521,13 +521,30 @@ __device__ __forceinline__ void row_scales(const float (&lmax)[M], int tid, int 
     if (lane == 0) s_scratch[m * kCW + warp] = __uint_as_float(wm);
   }
   dev::named_barrier_sync(kBarConsumers, kConsumers);
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const float4 a = *reinterpret_cast<const float4*>(s_scratch + m * kCW);
-    const float4 b = *reinterpret_cast<const float4*>(s_scratch + m * kCW + 4);
+  if constexpr (M == 1) {
+    const float4 a = *reinterpret_cast<const float4*>(s_scratch);
+    const float4 b = *reinterpret_cast<const float4*>(s_scratch + 4);
     const float amax = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
-    scale_and_rcp(amax, sc[m], rc[m]);
-    if (tid == 0) s_as[m] = sc[m];
+    scale_and_rcp(amax, sc[0], rc[0]);
+    if (tid == 0) s_as[0] = sc[0];
+  } else {
+    // thread m works out row m (the rows' chains in parallel, not one after another in every
+    // thread) and leaves the reciprocal in its row's first scratch slot
+    if (tid < M) {
+      const float4 a = *reinterpret_cast<const float4*>(s_scratch + tid * kCW);
+      const float4 b = *reinterpret_cast<const float4*>(s_scratch + tid * kCW + 4);
+      const float amax = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+      float s, r;
+      scale_and_rcp(amax, s, r);
+      s_as[tid] = s;
+      s_scratch[tid * kCW] = r;
+    }
+    dev::named_barrier_sync(kBarConsumers, kConsumers);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      sc[m] = s_as[m];
+      rc[m] = s_scratch[m * kCW];
+    }
   }
 }
 
@@ -565,6 +582,15 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
         const int k = 8 * tid + kStride * j;
         xv[m][j] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
       }
+#ifdef WOQ_TRACE
+    if (tid == 0 || tid == 224) {
+      uint32_t u = 0;
+#pragma unroll
+      for (int m = 0; m < M; ++m) u ^= xv[m][0].x;
+      asm volatile("" ::"r"(u));
+      WOQ_TRACE_EV2(tid == 0 ? 58 : 59);
+    }
+#endif
     if (amax_in) {  // the row amax is given: only the barrier (every x value read before any q byte is written)
       given_row_scales<M>(amax_in, tid, s_as, sc, rc);
     } else {
@@ -579,6 +605,12 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
         }
         lmax[m] = dev::bf16x2_absmax_to_float(acc);
       }
+#ifdef WOQ_TRACE
+      if (tid == 0 || tid == 224) {
+        asm volatile("" ::"f"(lmax[0]));
+        WOQ_TRACE_EV2(tid == 0 ? 60 : 61);
+      }
+#endif
       row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
     }
     if (tid == 0) WOQ_TRACE_EV2(5);
@@ -1176,6 +1208,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
     atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
   }
   asm volatile("" ::"r"(warm));
+  if (tid == 0) WOQ_TRACE_EV(57);
   if (tid == 0) {
     WOQ_TRACE_EV(4);
     // the packed header must describe this call's (bits, N, K)
