@@ -88,9 +88,9 @@ WOQ_API int woq_max_m(void);
 WOQ_API int woq_max_k(int bits, int M, int fused);
 
 /* ---------------------------------------------------------------------------
- * Packing (section "Optimizing the Linear Kernel": weights and their
- * per-group scales are interleaved in the order the kernel consumes them, so
- * each thread block streams one contiguous run).
+ * Packing (section "Optimizing the Linear Kernel": the GEMV reads weights and
+ * group scales from one buffer laid out in its reading order, one contiguous
+ * run per thread block).
  *
  * Canonical (checkpoint) layout, the input of the packers:
  *   int4: q4 uint8 [N][K/2]; weight (n, k) is the low nibble of byte k/2 when k
@@ -205,9 +205,9 @@ WOQ_API int woq_w6a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, cons
                          void* ws, size_t ws_bytes, woq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * Prologue fusions (section "Optimizing the Linear Kernel": the activation
- * quantisation absorbs the RMSNorm or SwiGLU that precedes the linear, so the
- * intermediate tensor is never written to memory).  One launch each; h is
+ * Prologue fusions (section "Optimizing the Linear Kernel": the RMSNorm or
+ * SwiGLU before a linear is folded into its input quantisation, so the tensor
+ * between them never goes to memory).  One launch each; h is
  * formed in shared memory, rounded to bf16, then quantised exactly as
  * woq_act_quant_int8 quantises x.
  *

@@ -6,8 +6,9 @@
  * few runner-up choices are kept as sibling leaves; the shape of the tree is a
  * chain of widths w_1 .. w_D with w_1 + ... + w_D = 7 (the 64 compositions of 7).
  * The planner keeps exponentially decayed counts of the rank the accepted token
- * had at each level (first choice, second, ..., seventh, or none), times the
- * draft and verify phases, and every 32 steps scores every shape by
+ * had at each level (first choice, second, ..., seventh, or none) and measured
+ * durations of the draft and verify phases; at each 32nd step it scores every
+ * shape by
  *
  *     expected tokens per step / (verify_ms + D * draft_ms)
  *

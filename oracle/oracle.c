@@ -241,7 +241,7 @@ int oracle_linear_bf16(int bits, const uint8_t* w, const uint16_t* wscale_f16, i
 
 /* ------------------------------------------------------------------------ */
 /* prologue fusions (R11 - R13; section "Optimizing the Linear Kernel": the  */
-/* activation quantisation absorbs the RMSNorm or SwiGLU that precedes it)   */
+/* RMSNorm or SwiGLU before a linear is folded into its input quantisation)  */
 /* ------------------------------------------------------------------------ */
 
 /* fp32 -> bf16 bit pattern, round to nearest, ties to even (finite inputs) */

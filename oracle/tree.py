@@ -10,9 +10,9 @@ the library's planner:
   choice continues the chain, choices 2 .. w_d are sibling leaves;
 - per level the planner keeps exponentially decayed counts of the rank the accepted
   token had (1 .. 7, or none), and decayed means of the draft and verify times;
-- every 32 steps it scores all 64 shapes by expected tokens per step divided by
-  verify_ms + D * draft_ms, and switches when the best beats the current shape by
-  at least 3 %.
+- at each 32nd step all 64 shapes get a score, expected tokens per step over
+  verify_ms + D * draft_ms, and the planner changes shape only for a winner at least
+  3 % above the current one.
 
 Readings where the section is silent (the same list is in include/woq_tree.h):
 counts at level d change only on steps that reached level d, so the estimated

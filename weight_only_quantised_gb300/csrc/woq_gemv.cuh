@@ -5,11 +5,11 @@
 //     per step with about one operation per weight, so the op is bound by the
 //     weight-read bandwidth of the memory;
 //   - "Optimizing the Linear Kernel": quantise the activation to int8, then a
-//     GEMV over weights whose group scales are interleaved with them in the
-//     order the kernel consumes them (each thread block streams one contiguous
-//     run); dp4a (CUDA-core int8 dot products) for the inner product;
-//   - "Paying attention to the attention!": the last block to finish combines
-//     the partial results inside the same launch (used here for split tiles).
+//     GEMV reading weights and their group scales from one buffer arranged in
+//     reading order (a contiguous run per thread block); dp4a (CUDA-core int8
+//     dot products) for the inner product;
+//   - "Paying attention to the attention!": partial results are merged inside
+//     the launch that produced them (used here for split tiles).
 //
 // GB300 design:
 //   * One CTA per SM (persistent).  The matrix's blocks (128 rows x 128 k) are

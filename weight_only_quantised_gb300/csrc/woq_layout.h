@@ -1,9 +1,9 @@
 // Packed device layout of the weight-only-quantised skinny linear.
 //
 // Section "Optimizing the Linear Kernel" of "Doubling LLM token rates in
-// ComfyUI": the weights and their per-group scales are interleaved in memory in
-// the order the kernel consumes them, so a thread block streams one contiguous
-// run instead of hopping between a weight tensor and a scale tensor.
+// ComfyUI": the GEMV reads weights and group scales from one buffer laid out in
+// its reading order, so each thread block streams a single contiguous run rather
+// than two separate tensors.
 //
 // This file fixes that order for the GB300 kernels:
 //

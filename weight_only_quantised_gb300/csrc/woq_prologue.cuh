@@ -1,7 +1,7 @@
 // Prologue fusions of the activation quantisation ("Doubling LLM token rates in
-// ComfyUI", section "Optimizing the Linear Kernel": the quantisation absorbs the
-// RMSNorm or SwiGLU that precedes the linear, so the intermediate tensor is never
-// written to memory).  Both produce bf16 h, which is then quantised exactly like a
+// ComfyUI", section "Optimizing the Linear Kernel": the RMSNorm or SwiGLU before a
+// linear is folded into its input quantisation, so the tensor between them never goes
+// to memory).  Both produce bf16 h, which is then quantised exactly like a
 // bf16 activation.  Every step is an IEEE fp32 operation (or integer arithmetic), so
 // the result is fixed bit for bit:
 //

@@ -305,8 +305,9 @@ __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __res
 }
 
 // ---------------------------------------------------------------------------
-// In-place relayout ("Optimizing the Linear Kernel": the re-layout is done in place in
-// VRAM, once per model load, with no extra RAM or VRAM).  The buffer holds, from byte
+// In-place relayout ("Optimizing the Linear Kernel": the weights are rearranged inside
+// the device buffer that holds them, once when the model is loaded, without a second
+// buffer on the device or the host).  The buffer holds, from byte
 // 256 on, the canonical weights (N rows) directly followed by the canonical fp16 scales;
 // it ends up holding the packed layout.  A packed tile t starts at 256 + t G BB, never
 // below the canonical bytes of any lower tile (G BB >= 128 row bytes), so the tiles are
