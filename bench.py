@@ -152,6 +152,37 @@ class ClockSampler:
                 "samples": len(sms), "power_w_max": max(powers)}
 
 
+# ----------------------------------------------------------------------------- ranks
+
+class RankGroup:
+    """The N replicas of a multi-GPU run: a barrier around the timed region and the maximum
+    of a per-rank time (no collective on the data path; replicas only).  device: where the
+    reduction tensor lives (the GPU under NCCL, the CPU under gloo)."""
+
+    def __init__(self, world, device):
+        self.world, self.device = world, device
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, v):
+        if self.world == 1:
+            return v
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+
+def job_value(world, bytes_per_step, ms_per_step):
+    """Whole-job throughput in GB/s: every replica streams bytes_per_step per step, and the
+    step time is the slowest replica's."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- our arm
 
 class Step:
@@ -343,17 +374,8 @@ def run_ours(args):
     device = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    group = RankGroup(world, device)
+    barrier, max_over_ranks = group.barrier, group.max
 
     do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     step = Step(device, cpu_sample_div=args.cpu_sample_div if do_cpu else 0)
@@ -365,7 +387,7 @@ def run_ours(args):
     ms_total, clocks = step.time_device(M, args.steps, args.warmup, barrier, sampler_gpu=gpu_index)
     ms_total = max_over_ranks(ms_total)
     ms_step = ms_total / args.steps
-    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    value = job_value(world, bytes_step, ms_step)
 
     extra = {}
     for em in [int(v) for v in args.extra_m.split(",") if v.strip()]:
