@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--linear", default="", help="time one 27B-class linear (qkv, o, gate_up, down, lm_head) "
                                                  "instead of the step: a graph of launches over distinct weight copies")
     ap.add_argument("--int8", action="store_true", help="with --linear: the int8 entry (act_quant once, then GEMV)")
+    ap.add_argument("--prologue", default="none", choices=["none", "rmsnorm", "swiglu"],
+                    help="with --linear: the bf16 entry with the RMSNorm prologue, or the SwiGLU entry")
     ap.add_argument("--tree-planner", action="store_true",
                     help="time one re-plan of the draft-tree planner (host code) against its oracle")
     ap.add_argument("--relayout", action="store_true",
@@ -556,10 +558,16 @@ def run_linear(args):
     woq.woq_act_quant_int8(x, q, a)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
     ws = torch.zeros(woq.woq_workspace_bytes(4, M, N, K), dtype=torch.uint8, device=dev)
+    gamma = synthetic.rmsnorm_weight(K, 9, device=dev)
+    gu = synthetic.gate_up_output(M, K, 9, device=dev)
 
     def launch(p):
         if args.int8:
             woq.woq_w4a8_gemv(p, q, a, N, K, y, ws)
+        elif args.prologue == "rmsnorm":
+            woq.woq_w4a8_linear_rmsnorm_bf16(p, x, gamma, 1e-6, N, K, y, ws)
+        elif args.prologue == "swiglu":
+            woq.woq_w4a8_linear_swiglu_f32(p, gu, N, K, y, ws)
         else:
             woq.woq_w4a8_linear_bf16(p, x, N, K, y, ws)
     st = torch.cuda.Stream()
@@ -580,9 +588,11 @@ def run_linear(args):
     e1.record()
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / (args.steps * copies)
-    nbytes = N * K // 2 + 2 * N * (K // 128) + (M * K if args.int8 else 2 * M * K)
+    act_bytes = {"none": 2 * M * K, "rmsnorm": 2 * M * K + 2 * K, "swiglu": 8 * M * K}[args.prologue]
+    nbytes = N * K // 2 + 2 * N * (K // 128) + (M * K if args.int8 else act_bytes)
     peak, kind = measured_peak()
-    print(json.dumps({"linear": args.linear, "K": K, "N": N, "m": M, "entry": "int8" if args.int8 else "bf16",
+    entry = "int8" if args.int8 else {"none": "bf16", "rmsnorm": "rmsnorm_bf16", "swiglu": "swiglu_f32"}[args.prologue]
+    print(json.dumps({"linear": args.linear, "K": K, "N": N, "m": M, "entry": entry,
                       "consumer": {0: "table", 1: "dp4a", 2: "mma"}[args.path],
                       "us_per_launch": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
                       "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "peak_kind": kind,
