@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--linear", default="", help="time one 27B-class linear (qkv, o, gate_up, down, lm_head) "
                                                  "instead of the step: a graph of launches over distinct weight copies")
     ap.add_argument("--int8", action="store_true", help="with --linear: the int8 entry (act_quant once, then GEMV)")
+    ap.add_argument("--bits", type=int, default=4, choices=[4, 6], help="with --linear: int4 or int6 weights")
     ap.add_argument("--prologue", default="none", choices=["none", "rmsnorm", "swiglu"],
                     help="with --linear: the bf16 entry with the RMSNorm prologue, or the SwiGLU entry")
     ap.add_argument("--tree-planner", action="store_true",
@@ -543,13 +544,14 @@ def run_linear(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     woq.woq_tune_path(args.path)
-    pb = woq.woq_packed_bytes(4, N, K)
+    bits = args.bits
+    pb = woq.woq_packed_bytes(bits, N, K)
     copies = max(4, int(1.2e9 // pb))
-    w, s = synthetic.weights(4, N, K, synthetic.sub_seed(2, args.linear), device=dev)
+    w, s = synthetic.weights(bits, N, K, synthetic.sub_seed(2, args.linear), device=dev)
     bufs = []
     for _ in range(copies):
         p = torch.empty(pb, dtype=torch.uint8, device=dev)
-        woq.woq_pack_device(4, w, s.view(torch.int16), N, K, p)
+        woq.woq_pack_device(bits, w, s.view(torch.int16), N, K, p)
         bufs.append(p)
     del w, s
     x = synthetic.activations(M, K, synthetic.sub_seed(2, "x", M, K), device=dev)
@@ -557,19 +559,22 @@ def run_linear(args):
     a = torch.empty((M,), dtype=torch.float32, device=dev)
     woq.woq_act_quant_int8(x, q, a)
     y = torch.empty((M, N), dtype=torch.float32, device=dev)
-    ws = torch.zeros(woq.woq_workspace_bytes(4, M, N, K), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(woq.woq_workspace_bytes(bits, M, N, K), dtype=torch.uint8, device=dev)
     gamma = synthetic.rmsnorm_weight(K, 9, device=dev)
     gu = synthetic.gate_up_output(M, K, 9, device=dev)
 
+    w4 = bits == 4
+
     def launch(p):
         if args.int8:
-            woq.woq_w4a8_gemv(p, q, a, N, K, y, ws)
+            (woq.woq_w4a8_gemv if w4 else woq.woq_w6a8_gemv)(p, q, a, N, K, y, ws)
         elif args.prologue == "rmsnorm":
-            woq.woq_w4a8_linear_rmsnorm_bf16(p, x, gamma, 1e-6, N, K, y, ws)
+            (woq.woq_w4a8_linear_rmsnorm_bf16 if w4 else woq.woq_w6a8_linear_rmsnorm_bf16)(p, x, gamma, 1e-6, N, K,
+                                                                                         y, ws)
         elif args.prologue == "swiglu":
-            woq.woq_w4a8_linear_swiglu_f32(p, gu, N, K, y, ws)
+            (woq.woq_w4a8_linear_swiglu_f32 if w4 else woq.woq_w6a8_linear_swiglu_f32)(p, gu, N, K, y, ws)
         else:
-            woq.woq_w4a8_linear_bf16(p, x, N, K, y, ws)
+            (woq.woq_w4a8_linear_bf16 if w4 else woq.woq_w6a8_linear_bf16)(p, x, N, K, y, ws)
     st = torch.cuda.Stream()
     with torch.cuda.stream(st):
         launch(bufs[0])
@@ -589,10 +594,10 @@ def run_linear(args):
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / (args.steps * copies)
     act_bytes = {"none": 2 * M * K, "rmsnorm": 2 * M * K + 2 * K, "swiglu": 8 * M * K}[args.prologue]
-    nbytes = N * K // 2 + 2 * N * (K // 128) + (M * K if args.int8 else act_bytes)
+    nbytes = N * K * bits // 8 + 2 * N * (K // 128) + (M * K if args.int8 else act_bytes)
     peak, kind = measured_peak()
     entry = "int8" if args.int8 else {"none": "bf16", "rmsnorm": "rmsnorm_bf16", "swiglu": "swiglu_f32"}[args.prologue]
-    print(json.dumps({"linear": args.linear, "K": K, "N": N, "m": M, "entry": entry,
+    print(json.dumps({"linear": args.linear, "K": K, "N": N, "m": M, "bits": bits, "entry": entry,
                       "consumer": {0: "table", 1: "dp4a", 2: "mma"}[args.path],
                       "us_per_launch": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
                       "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "peak_kind": kind,
