@@ -380,13 +380,29 @@ __global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, Rela
     const int tlo = thi > pl.tiles_per_batch ? thi - pl.tiles_per_batch : 0;
     const int nb = (thi - tlo) * pl.G;
     const int i_lo = (int)((long long)cta * nb / C), i_hi = (int)((long long)(cta + 1) * nb / C);
-    for (int i = i_lo; i < i_hi; ++i, ++slot) {
-      const int b = tlo * pl.G + i, t = b / pl.G, g = b % pl.G;
-      for (int r = tid; r < kTileRows; r += kRlThreads) {
-        const int n = t * kTileRows + r;
-        s_scales[slot * kTileRows + scale_index(r)] = n < pl.N ? canon_s[(size_t)n * pl.G + g] : (uint16_t)0;
+    // thread (block offset tid / 128, row tid % 128): four blocks per pass, kSU passes' loads
+    // in flight before their stores
+    constexpr int kBPP = kRlThreads / kTileRows, kSU = 8;
+    const int r = tid % kTileRows;
+    for (int i0 = i_lo; i0 < i_hi; i0 += kBPP * kSU) {
+      uint16_t v[kSU];
+#pragma unroll
+      for (int u = 0; u < kSU; ++u) {
+        const int i = i0 + u * kBPP + tid / kTileRows;
+        v[u] = 0;
+        if (i < i_hi) {
+          const int b = tlo * pl.G + i, t = b / pl.G, g = b % pl.G;
+          const int n = t * kTileRows + r;
+          if (n < pl.N) v[u] = canon_s[(size_t)n * pl.G + g];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kSU; ++u) {
+        const int i = i0 + u * kBPP + tid / kTileRows;
+        if (i < i_hi) s_scales[(slot + (i - i_lo)) * kTileRows + scale_index(r)] = v[u];
       }
     }
+    slot += i_hi - i_lo;
   }
   if (!rl_grid_barrier(words, &s_ok)) return;
 
@@ -399,7 +415,7 @@ __global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, Rela
     const int nb = (thi - tlo) * pl.G;
     const int i_lo = (int)((long long)cta * nb / C), i_hi = (int)((long long)(cta + 1) * nb / C);
     // gather, converted to the packed order; kUnroll blocks' loads in flight before converting
-    constexpr int kUnroll = 4;
+    constexpr int kUnroll = 8;
     for (int i0 = i_lo, k0 = 0; i0 < i_hi; i0 += kUnroll, k0 += kUnroll) {
       RawChunk raw[kUnroll];
 #pragma unroll
