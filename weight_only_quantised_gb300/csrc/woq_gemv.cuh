@@ -84,7 +84,9 @@ struct GemvParams {
 // Trace build only: %globaltimer stamps per (launch slot, CTA, event); no atomics.
 constexpr int kTraceSlots = 16;
 constexpr int kTraceCtas = 512;
-constexpr int kTraceEvents = 64;  // 0..15 phases, 16+s stage s ready (warp 0), 32+i ring load i issued, 48.. combine
+// events: 0..15 phases, 16+s stage s ready (warp 0), 32+i ring load i issued, 48.. combine,
+// 56 before the grid wait, 59 / 58 around the split-tile roles, 60..63 prologue phases
+constexpr int kTraceEvents = 64;
 static __device__ unsigned long long g_trace[kTraceSlots * kTraceCtas * kTraceEvents];
 #define WOQ_TRACE_EV(ev)                                                                              \
   do {                                                                                                \
@@ -582,15 +584,6 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
         const int k = 8 * tid + kStride * j;
         xv[m][j] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
       }
-#ifdef WOQ_TRACE
-    if (tid == 0 || tid == 224) {
-      uint32_t u = 0;
-#pragma unroll
-      for (int m = 0; m < M; ++m) u ^= xv[m][0].x;
-      asm volatile("" ::"r"(u));
-      WOQ_TRACE_EV2(tid == 0 ? 58 : 59);
-    }
-#endif
     if (amax_in) {  // the row amax is given: only the barrier (every x value read before any q byte is written)
       given_row_scales<M>(amax_in, tid, s_as, sc, rc);
     } else {
@@ -605,12 +598,6 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
         }
         lmax[m] = dev::bf16x2_absmax_to_float(acc);
       }
-#ifdef WOQ_TRACE
-      if (tid == 0 || tid == 224) {
-        asm volatile("" ::"f"(lmax[0]));
-        WOQ_TRACE_EV2(tid == 0 ? 60 : 61);
-      }
-#endif
       row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
     }
     if (tid == 0) WOQ_TRACE_EV2(5);
@@ -1208,7 +1195,6 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
     atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
   }
   asm volatile("" ::"r"(warm));
-  if (tid == 0) WOQ_TRACE_EV(57);
   if (tid == 0) {
     WOQ_TRACE_EV(4);
     // the packed header must describe this call's (bits, N, K)
