@@ -86,7 +86,7 @@ def _run(fn, *args):
 
 @pytest.mark.parametrize("bits,path", BITS_PATHS)
 @pytest.mark.parametrize("M", [1, 3, 4])
-@pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (2048, 5120), (700, 6144), (700, 6272)])
+@pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (2048, 5120), (700, 6144), (700, 6272), (64, 256)])
 def test_fused_rmsnorm_linear(bits, path, M, N, K):
     """K = 6144 is the largest row the fused RMSNorm keeps in registers (M <= 4); 6272 takes
     the shared-memory passes."""
@@ -117,8 +117,9 @@ def test_fused_rmsnorm_linear(bits, path, M, N, K):
 
 @pytest.mark.parametrize("bits,path", BITS_PATHS)
 @pytest.mark.parametrize("M", [1, 3, 4])
-@pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (640, 5120)])
+@pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (640, 5120), (64, 256)])
 def test_fused_swiglu_linear(bits, path, M, N, K):
+    """(64, 256) is two blocks: a grid of one CTA, whose grid-wide maximum is its own."""
     woq.woq_tune_path(path)
     w, s = synthetic.weights(bits, N, K, seed=5 * N + K + bits)
     wn, sn = to_numpy_u8(w), to_numpy_u16(s)
