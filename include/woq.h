@@ -282,6 +282,15 @@ WOQ_API int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_b
  * --------------------------------------------------------------------------- */
 WOQ_API int woq_tune_override(int ctas_per_sm, int stages, int prefetch_kb);
 
+/* The cudaError_t code of the most recent CUDA runtime call that failed inside the
+ * library on this thread (an entry returned WOQ_ERR_CUDA), or 0.  The library
+ * clears the runtime's own error state after such a failure, so it does not
+ * surface again in a later call. */
+WOQ_API int woq_last_cuda_error(void);
+
+/* cudaGetErrorName of a code returned by woq_last_cuda_error (static string). */
+WOQ_API const char* woq_cuda_error_name(int code);
+
 /* Tuning: which consumer the following int4 GEMV / linear launches of this process
  * use: 0 = launch table (dp4a), 1 = dp4a, 2 = f16 tensor-core MMA.  Both form the
  * same exact per-group integer dots; outputs agree within the GEMV tolerance.

@@ -63,6 +63,8 @@ _SIGS = {
     "woq_w4a8_linear_bf16_noalloc": ([_P, _Z, _P, _I, _I, _I, _P, _P], _I),
     "woq_tune_override": ([_I, _I, _I], _I),
     "woq_tune_path": ([_I], _I),
+    "woq_last_cuda_error": ([], _I),
+    "woq_cuda_error_name": ([_I], ctypes.c_char_p),
     "woq_w4a8_linear_rmsnorm_bf16": ([_P, _Z, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _Z, _P], _I),
     "woq_w6a8_linear_rmsnorm_bf16": ([_P, _Z, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _Z, _P], _I),
     "woq_w4a8_linear_swiglu_f32": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
@@ -79,7 +81,11 @@ for _name, (_args, _res) in _SIGS.items():
 class WoqError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {lib.woq_status_string(status).decode()} (status {status})")
+        msg = f"{what}: {lib.woq_status_string(status).decode()} (status {status})"
+        if status == WOQ_ERR_CUDA:
+            code = lib.woq_last_cuda_error()
+            msg += f" [{lib.woq_cuda_error_name(code).decode()}]"
+        super().__init__(msg)
 
 
 def _check(status: int, what: str) -> None:

@@ -22,9 +22,22 @@ std::atomic<int> g_override_prefetch_kb{-1};
 std::atomic<int> g_override_path{0};  // 0: table, else 1 + kern::Consumer
 std::atomic<int> g_launch_counter{0};  // numbers GEMV launches (trace builds key their stamps by it)
 
+// A failed CUDA call: remembered for woq_last_cuda_error (per thread) and cleared from the
+// runtime's error state, so that it does not surface again in the caller's next call.
+thread_local int t_last_cuda_error = 0;
+int cuda_result(cudaError_t e) {
+  if (e == cudaSuccess) return WOQ_OK;
+  t_last_cuda_error = (int)e;
+  (void)cudaGetLastError();
+  return WOQ_ERR_CUDA;
+}
+
 int current_device() {
   int d = 0;
-  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  if (const cudaError_t e = cudaGetDevice(&d); e != cudaSuccess) {
+    cuda_result(e);
+    return -1;
+  }
   return d;
 }
 
@@ -188,6 +201,10 @@ const char* woq_status_string(int status) {
   }
 }
 
+int woq_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* woq_cuda_error_name(int code) { return cudaGetErrorName((cudaError_t)code); }
+
 int woq_tune_override(int ctas_per_sm, int stages, int prefetch_kb) {
   if (ctas_per_sm < 0 || ctas_per_sm > 2 || stages < 0 || stages == 1 || stages > kMaxStages || prefetch_kb < -1 ||
       prefetch_kb > 65536)
@@ -224,7 +241,7 @@ size_t woq_workspace_bytes(int bits, int M, int N, int K) {
 int woq_workspace_init(void* ws_dev, size_t ws_bytes, woq_stream_t stream) {
   if (!ws_dev) return WOQ_ERR_NULL;
   if (!aligned(ws_dev, 16)) return WOQ_ERR_ALIGN;
-  return cudaMemsetAsync(ws_dev, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+  return cuda_result(cudaMemsetAsync(ws_dev, 0, ws_bytes, (cudaStream_t)stream));
 }
 
 int woq_read_status(void* ws_dev, size_t ws_bytes, int clear, uint32_t* status_out, woq_stream_t stream) {
@@ -232,11 +249,12 @@ int woq_read_status(void* ws_dev, size_t ws_bytes, int clear, uint32_t* status_o
   if (ws_bytes < 4) return WOQ_ERR_WORKSPACE;
   uint32_t v = 0;
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(&v, ws_dev, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return WOQ_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return WOQ_ERR_CUDA;
+  if (const cudaError_t e_ = cudaMemcpyAsync(&v, ws_dev, 4, cudaMemcpyDeviceToHost, s); e_ != cudaSuccess)
+    return cuda_result(e_);
+  if (const cudaError_t e_ = cudaStreamSynchronize(s); e_ != cudaSuccess) return cuda_result(e_);
   if (clear && v) {
-    if (cudaMemsetAsync(ws_dev, 0, 4, s) != cudaSuccess) return WOQ_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return WOQ_ERR_CUDA;
+    if (const cudaError_t e_ = cudaMemsetAsync(ws_dev, 0, 4, s); e_ != cudaSuccess) return cuda_result(e_);
+    if (const cudaError_t e_ = cudaStreamSynchronize(s); e_ != cudaSuccess) return cuda_result(e_);
   }
   *status_out = v;
   return WOQ_OK;
@@ -249,9 +267,7 @@ int woq_pack_device(int bits, const uint8_t* q_dev, const uint16_t* scales_dev, 
   if (!dst_dev || ((!q_dev || !scales_dev) && (size_t)N * (size_t)K > 0)) return WOQ_ERR_NULL;
   if (!aligned(dst_dev, 16) || !aligned(q_dev, 16) || !aligned(scales_dev, 2)) return WOQ_ERR_ALIGN;
   if (dst_bytes < need) return WOQ_ERR_LAYOUT;
-  return launch_pack_device(bits, q_dev, scales_dev, N, K, dst_dev, (cudaStream_t)stream) == cudaSuccess
-             ? WOQ_OK
-             : WOQ_ERR_CUDA;
+  return cuda_result(launch_pack_device(bits, q_dev, scales_dev, N, K, dst_dev, (cudaStream_t)stream));
 }
 
 int woq_relayout_inplace(int bits, void* buf, size_t buf_bytes, int N, int K, woq_stream_t stream) {
@@ -265,7 +281,7 @@ int woq_relayout_inplace(int bits, void* buf, size_t buf_bytes, int N, int K, wo
     write_header(h, bits, N, K);
     cudaError_t e = cudaMemcpyAsync(buf, h, kHeaderBytes, cudaMemcpyHostToDevice, (cudaStream_t)stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
-    return e == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+    return cuda_result(e);
   }
   int too_large = 0;
   cudaError_t e = launch_relayout(bits, buf, N, K, &too_large, (cudaStream_t)stream);
@@ -273,7 +289,7 @@ int woq_relayout_inplace(int bits, void* buf, size_t buf_bytes, int N, int K, wo
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
   uint32_t head[4] = {0u, 0u, 0u, 0u};
   if (e == cudaSuccess) e = cudaMemcpy(head, buf, sizeof(head), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return WOQ_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_result(e);
   return head[0] == kMagic ? WOQ_OK : WOQ_ERR_DEVICE;
 }
 
@@ -282,7 +298,7 @@ int woq_act_quant_int8(const void* x_bf16, int M, int K, int8_t* q, float* ascal
   if (M == 0) return WOQ_OK;
   if (!ascale || (K > 0 && (!x_bf16 || !q))) return WOQ_ERR_NULL;
   if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(ascale, 4)) return WOQ_ERR_ALIGN;
-  return launch_act_quant(x_bf16, M, K, q, ascale, (cudaStream_t)stream) == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+  return cuda_result(launch_act_quant(x_bf16, M, K, q, ascale, (cudaStream_t)stream));
 }
 
 int woq_rmsnorm_act_quant_int8(const void* x_bf16, const void* gamma_bf16, float eps, int M, int K, int8_t* q,
@@ -292,10 +308,8 @@ int woq_rmsnorm_act_quant_int8(const void* x_bf16, const void* gamma_bf16, float
   if (M == 0) return WOQ_OK;
   if (!ascale || (K > 0 && (!x_bf16 || !q || !gamma_bf16))) return WOQ_ERR_NULL;
   if (!aligned(x_bf16, 16) || !aligned(gamma_bf16, 16) || !aligned(q, 16) || !aligned(ascale, 4)) return WOQ_ERR_ALIGN;
-  return launch_pro_act_quant(kern::kProRms, x_bf16, static_cast<const uint16_t*>(gamma_bf16), eps, M, K, q, ascale,
-                              (cudaStream_t)stream) == cudaSuccess
-             ? WOQ_OK
-             : WOQ_ERR_CUDA;
+  return cuda_result(launch_pro_act_quant(kern::kProRms, x_bf16, static_cast<const uint16_t*>(gamma_bf16), eps, M, K, q,
+                                          ascale, (cudaStream_t)stream));
 }
 
 int woq_swiglu_act_quant_int8(const float* gate_up, int M, int K, int8_t* q, float* ascale, woq_stream_t stream) {
@@ -303,10 +317,7 @@ int woq_swiglu_act_quant_int8(const float* gate_up, int M, int K, int8_t* q, flo
   if (M == 0) return WOQ_OK;
   if (!ascale || (K > 0 && (!gate_up || !q))) return WOQ_ERR_NULL;
   if (!aligned(gate_up, 16) || !aligned(q, 16) || !aligned(ascale, 4)) return WOQ_ERR_ALIGN;
-  return launch_pro_act_quant(kern::kProSwiglu, gate_up, nullptr, 0.0f, M, K, q, ascale, (cudaStream_t)stream) ==
-                 cudaSuccess
-             ? WOQ_OK
-             : WOQ_ERR_CUDA;
+  return cuda_result(launch_pro_act_quant(kern::kProSwiglu, gate_up, nullptr, 0.0f, M, K, q, ascale, (cudaStream_t)stream));
 }
 
 // pro: kern::Prologue.  x: bf16 [M][K] (bf16, RMSNorm) or fp32 [M][2K] (SwiGLU).
@@ -319,7 +330,7 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   if (!y) return WOQ_ERR_NULL;
   if (!aligned(y, 4)) return WOQ_ERR_ALIGN;
   if (K == 0) {  // no groups: every output is the empty sum
-    return cudaMemsetAsync(y, 0, (size_t)M * N * sizeof(float), stream) == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+    return cuda_result(cudaMemsetAsync(y, 0, (size_t)M * N * sizeof(float), stream));
   }
   if (!wpacked || !ws) return WOQ_ERR_NULL;
   if (fused ? !x : (!q || !ascale)) return WOQ_ERR_NULL;
@@ -365,7 +376,7 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   p.ring_offset = ring_offset(M, K, fused, cfg.consumer);
   p.launch_id = g_launch_counter.fetch_add(1, std::memory_order_relaxed) & 0x7fffffff;
   const cudaError_t e = launch_gemv_any(bits, pro, cfg.consumer, M, p, cfg, stream);
-  return e == cudaSuccess ? WOQ_OK : WOQ_ERR_CUDA;
+  return cuda_result(e);
 }
 
 int woq_w4a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
@@ -425,8 +436,7 @@ int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_bytes, co
   if (!wpacked || !q || !dots) return WOQ_ERR_NULL;
   if (!aligned(wpacked, 16) || !aligned(q, 16) || !aligned(dots, 4)) return WOQ_ERR_ALIGN;
   if (wpacked_bytes < packed_bytes(bits, N, K)) return WOQ_ERR_LAYOUT;
-  return launch_group_dots(bits, wpacked, q, M, N, K, dots, (cudaStream_t)stream) == cudaSuccess ? WOQ_OK
-                                                                                                  : WOQ_ERR_CUDA;
+  return cuda_result(launch_group_dots(bits, wpacked, q, M, N, K, dots, (cudaStream_t)stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -455,7 +465,8 @@ static int noalloc_scratch(void** out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   if (g_noalloc_ptr[d] == nullptr) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return WOQ_ERR_CUDA;
+    if (const cudaError_t e_ = cudaGetSymbolAddress(&ptr, g_noalloc_scratch); e_ != cudaSuccess) return cuda_result(e_);
+    if (ptr == nullptr) return WOQ_ERR_CUDA;
     g_noalloc_ptr[d] = ptr;
   }
   *out = g_noalloc_ptr[d];
@@ -488,7 +499,7 @@ int woq_w4a8_linear_bf16_noalloc(const void* wpacked, size_t wpacked_bytes, cons
   const int st = noalloc_scratch(&ws);
   if (st != WOQ_OK) return st;
   // the array keeps the previous call's contents: start from zero (no allocation involved)
-  if (cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream) != cudaSuccess) return WOQ_ERR_CUDA;
+  if (const cudaError_t e_ = cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream); e_ != cudaSuccess) return cuda_result(e_);
   return run_gemv(4, kern::kProBf16, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, nullptr, 0.0f, M, N, K, y, ws,
                   kNoAllocScratchBytes, (cudaStream_t)stream);
 }
