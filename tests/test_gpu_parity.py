@@ -204,6 +204,31 @@ def test_fused_linear_matches_oracle_and_separate_path(bits, path, M, N, K, cons
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
+# The fused entry reads rows that fit registers (up to 12 vectors of 8 values per thread over the
+# M rows) straight from global memory for M <= 3, and copies longer rows (and every M = 4 row) into
+# shared memory first: both sides of each limit, against the oracle and the separate path.
+@pytest.mark.parametrize("bits", [4, 6])
+@pytest.mark.parametrize("M,K", [(1, 24576), (1, 24704), (2, 12288), (2, 12416), (3, 8192), (3, 8320),
+                                 (4, 6144), (4, 6272)])
+def test_fused_linear_register_limit(bits, M, K):
+    N = 300
+    w, s = make_weights(bits, N, K, seed=17 * K + M + bits)
+    wn, sn = to_numpy_u8(w), to_numpy_u16(s)
+    x = synthetic.activations(M, K, seed=3 * K + M, outliers=True)
+    xn = to_numpy_u16(x)
+    y_ref, S = oracle.linear_bf16(bits, wn, sn, N, K, xn)
+    wdev = pack_host(bits, wn, sn, N, K)
+    x_dev = torch.from_numpy(xn.view(np.int16)).to(DEV).view(torch.bfloat16)
+    y = run_linear(bits, wdev, x_dev, N, K, M)
+    ok, worst = tol_ok(y, y_ref, S)
+    assert ok, f"max err / tolerance = {worst}"
+    q = torch.empty((M, K), dtype=torch.int8, device=DEV)
+    a = torch.empty((M,), dtype=torch.float32, device=DEV)
+    woq.woq_act_quant_int8(x_dev, q, a)
+    y2 = run_gemv(bits, wdev, q, a, N, K, M)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
 # M = 5 .. 8 (int4 only): the launch table runs the tensor-core consumer
 @pytest.mark.parametrize("M", [5, 6, 7, 8])
 @pytest.mark.parametrize("N,K", [(1000, 1024), (300, 384), (129, 128), (640, 2048)])

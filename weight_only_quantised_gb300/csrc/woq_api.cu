@@ -111,8 +111,13 @@ int smem_bytes_for(int bits, int M, int K, bool fused, int stages) {
   return ring_offset(M, K, fused, choose_consumer(bits, M)) + stages * kStageBlocks * block_bytes(bits);
 }
 
-// Two CTAs (of this launch and the next) share an SM when each needs at most this much.
-static constexpr int kCoResidentBudget = (233472 - 2 * 1024) / 2;
+// Shared memory a launch's ring and activations may take by default.  The kernel runs one CTA
+// per SM (nine warps at 112 registers: the 16,384-register file of a sub-partition holds four
+// such warps, so a second CTA never fits), and the next launch's CTA takes over an SM as soon
+// as this launch's CTA there exits.  A ring deeper than this budget puts more of the next
+// launch's weights in the memory queues ahead of the running launch's activation and partial
+// reads: 27B step at M = 1 2.33 ms, 2.40-2.41 ms with four to seven stages everywhere.
+static constexpr int kRingBudget = (233472 - 2 * 1024) / 2;
 
 LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
   LaunchConfig cfg = {0, 0, 0, 0, 0};
@@ -127,12 +132,15 @@ LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
   if (cps <= 0) cps = 1;
   int stages = g_override_stages.load(std::memory_order_relaxed);
   if (stages > 0) {
-    const int budget = cps == 1 ? smem_max : kCoResidentBudget;
+    const int budget = cps == 1 ? smem_max : kRingBudget;
     while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > budget) --stages;
   } else {
-    // prefer a ring small enough for co-residency with the next launch, else the largest that fits
+    // up to four stages within the ring budget, else the largest ring that fits.  Two rows take
+    // four stages wherever they fit (within the budget their 2 M K byte activations leave some
+    // linears only two stages): 27B step at M = 2 2.722 ms against 2.760 ms.
+    const int budget = M == 2 ? smem_max : kRingBudget;
     stages = 4;
-    while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > kCoResidentBudget) --stages;
+    while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > budget) --stages;
     if (stages < 2 && cps == 1) {
       stages = 4;
       while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > smem_max) --stages;

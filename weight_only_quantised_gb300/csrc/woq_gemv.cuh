@@ -25,9 +25,9 @@
 //     whole stages (4 consecutive blocks of one tile, 33 KB for int4) into a
 //     small ring of shared-memory stages tracked by mbarriers (L2 evict-first:
 //     every weight byte is read once), and keeps a short window of later stages
-//     in flight from HBM into L2 with bulk L2 prefetches.  The small ring lets
-//     the CTA of the next launch share the SM and start its weight stream
-//     before this one ends.
+//     in flight from HBM into L2 with bulk L2 prefetches.  The CTA of the next
+//     launch takes over the SM as soon as this one exits and starts its weight
+//     stream before the whole grid has ended.
 //   * Warps 0..7 consume: warp w takes rows 64(w&1) .. 64(w&1)+63 of block w>>1
 //     of each stage.  Lane l owns two rows of that half; for each 32-k quarter
 //     it reads its 16-byte chunk per row (consecutive lanes, conflict-free) and
@@ -36,9 +36,11 @@
 //     dp4a.  Per group the int32 dot is exact; the term (d * wscale) * ascale is
 //     formed with two fp32 roundings, as in the definition, and accumulated in
 //     fp32.
-//   * The activations arrive with one bulk copy and stay in shared memory for the
-//     whole launch.  The fused entry copies bf16 x, takes the per-row amax and
-//     quantises it in place, bit-identical to the standalone kernel.
+//   * The activations stay in shared memory (as int8 q) for the whole launch.
+//     The int8 entry copies q with one bulk copy.  The fused entry reads bf16 x
+//     (straight into registers for up to three rows that fit them, else with a
+//     bulk copy), takes the per-row amax and quantises it, bit-identical to the
+//     standalone kernel.
 //   * Programmatic dependent launch: the producer streams weights before the
 //     previous kernel in the stream has finished; the activation copy, and every
 //     write to y or the workspace, wait for it (griddepcontrol.wait).
@@ -567,10 +569,14 @@ __device__ __forceinline__ void given_row_scales(const float* amax_in, int tid, 
 // all-zero row has rc = 0), else zero so that every vector of the row is redone.
 __device__ __forceinline__ uint32_t row_gate(float rc) { return rc <= 3.4028234e38f ? 0xFFFFFFFFu : 0u; }
 
-template <int M>
+// X_GLOBAL: rows that fit registers are read straight from x in global memory (L2 only: the
+// previous grid wrote them) instead of from a bf16 copy in shared memory; longer rows are not
+// taken that way (the caller copies them).
+template <int M, bool X_GLOBAL = false>
 __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, int klo1, int khi1, int klo2, int khi2,
                                                   int tid, int lane, int warp, float* s_scratch, float* s_as,
-                                                  int launch_id, const float* amax_in = nullptr) {
+                                                  int launch_id, const float* amax_in = nullptr,
+                                                  const uint16_t* xg = nullptr) {
   constexpr int kVPR = kRegVecs / M;  // vectors per row held in registers
   constexpr int kStride = kConsumers * 8;  // values per vector round of all threads
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
@@ -582,7 +588,10 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
 #pragma unroll
       for (int j = 0; j < kVPR; ++j) {
         const int k = 8 * tid + kStride * j;
-        xv[m][j] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
+        if constexpr (X_GLOBAL)
+          xv[m][j] = k < K ? __ldcg(reinterpret_cast<const uint4*>(xg + (size_t)m * K + k)) : make_uint4(0, 0, 0, 0);
+        else
+          xv[m][j] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
       }
     if (amax_in) {  // the row amax is given: only the barrier (every x value read before any q byte is written)
       given_row_scales<M>(amax_in, tid, s_as, sc, rc);
@@ -990,7 +999,10 @@ __device__ __forceinline__ bool swiglu_sync_reset(uint32_t* sync, uint32_t C) {
 enum Consumer { kDp4a = 0, kMma = 1 };
 
 template <int BITS, int M, int PRO, int CONS>
-__global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 288 threads x 112 fit one SM
+// 112 registers: one CTA per SM (a sub-partition's 16,384 registers hold four such warps, and
+// nine warps put three on one).  80, which lets two CTAs share an SM, spills and was slower
+// (27B step: M = 1 2.47 against 2.33 ms, M = 2 3.53 against 2.76 ms).
+__global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
   constexpr bool FUSED = PRO != kProInt8;  // activations quantised inside this launch
   static_assert(CONS == kDp4a || BITS == 4, "the tensor-core consumer reads int4 blocks");
   static_assert(CONS == kMma || M <= kMaxMDp4a, "dp4a kernels take up to four activation rows");
@@ -1169,13 +1181,19 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
     hdr1 = __ldg(reinterpret_cast<const uint4*>(p.w + 16));
   }
   if (tid == 0) WOQ_TRACE_EV(56);
+  // bf16 rows that fit registers are read by the consumers themselves after the grid wait (no
+  // bulk copy and mbarrier round trip on the launch's critical path).  27B step: M = 1 2.337 ->
+  // 2.309 ms, M = 2 2.731 -> 2.703, M = 3 3.214 -> 3.200; M = 4 went the other way (3.663 ->
+  // 3.726) and keeps the bulk copy.
+  constexpr bool kXDirect = PRO == kProBf16 && M <= 3;
+  const bool x_direct = kXDirect && p.K <= kConsumers * 8 * (kRegVecs / M);
   // activations (and y, the workspace) belong to the previous grid until it has completed
   dev::pdl_wait_prior_grids();
   if (tid == 0) {
     WOQ_TRACE_EV(3);
     const uint32_t act_bytes = (uint32_t)(FUSED ? 2 * M * p.K : M * p.K);
-    if (PRO == kProSwiglu) {
-      dev::mbar_arrive(actbar);  // nothing to copy: the consumers read the fp32 rows themselves
+    if (PRO == kProSwiglu || x_direct) {
+      dev::mbar_arrive(actbar);  // nothing to copy: the consumers read the rows themselves
     } else if (FUSED || p.act_stride == p.K) {
       dev::mbar_arrive_expect_tx(actbar, act_bytes);
       dev::bulk_copy_g2s(act, FUSED ? p.x : static_cast<const void*>(p.q), act_bytes, actbar);
@@ -1230,6 +1248,13 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {  // 2 CTAs x 
         atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
       }
     }
+  } else if constexpr (PRO == kProBf16) {
+    if (kXDirect && x_direct)
+      quantise_prologue<M, kXDirect>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
+                                 p.launch_id, nullptr, static_cast<const uint16_t*>(p.x));
+    else
+      quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
+                           p.launch_id);
   } else if constexpr (FUSED) {
     if (!quantised)
       quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
