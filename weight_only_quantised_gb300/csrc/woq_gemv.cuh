@@ -1294,7 +1294,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
 
     for (int g0 = ga; g0 < gb; g0 += kSB) {
       const int nb = gb - g0 < kSB ? gb - g0 : kSB;
-      // (the verdict is made warp-uniform: the tensor-core consumer shuffles across the warp)
+      // (the outcome is made warp-uniform: the tensor-core consumer shuffles across the warp)
       if (!aborted && !__all_sync(0xffffffffu, dev::mbar_wait_bounded(full + slot, phase))) {
         aborted = true;
         s_flags[1] = 1;
