@@ -112,3 +112,25 @@ def test_linear_and_act_quant_host_validation(woq):
     assert L.woq_tune_override(0, 1, -1) == woq.WOQ_ERR_SHAPE
     assert L.woq_tune_override(0, 0, -2) == woq.WOQ_ERR_SHAPE
     assert L.woq_tune_override(0, 0, -1) == woq.WOQ_OK
+
+
+def test_cuda_failure_is_reported_and_cleared(woq):
+    """Without a GPU every CUDA runtime call fails: the entry returns WOQ_ERR_CUDA, the failing
+    code is kept for woq_last_cuda_error (and named by woq_cuda_error_name), and the binding's
+    exception carries the name.  Skipped where a GPU is present (no invalid pointer ever reaches
+    a device)."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU")
+    L = woq.lib
+    P = ctypes.c_void_p
+    assert L.woq_cuda_error_name(0) == b"cudaSuccess"
+    assert L.woq_workspace_init(P(FAKE), 256, None) == woq.WOQ_ERR_CUDA
+    code = L.woq_last_cuda_error()
+    assert code != 0
+    assert L.woq_cuda_error_name(code).startswith(b"cudaError")
+    # host-side validation still answers first and leaves the recorded code alone
+    assert L.woq_workspace_init(None, 256, None) == woq.WOQ_ERR_NULL
+    assert L.woq_last_cuda_error() == code
+    with pytest.raises(woq.WoqError, match=r"\[cudaError\w+\]"):
+        woq._check(L.woq_workspace_init(P(FAKE), 256, None), "woq_workspace_init")
