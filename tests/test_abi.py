@@ -134,3 +134,21 @@ def test_cuda_failure_is_reported_and_cleared(woq):
     assert L.woq_last_cuda_error() == code
     with pytest.raises(woq.WoqError, match=r"\[cudaError\w+\]"):
         woq._check(L.woq_workspace_init(P(FAKE), 256, None), "woq_workspace_init")
+
+
+def test_binding_refuses_host_tensors(woq):
+    """The Python entries hand bare pointers to the library: a tensor that is not on the GPU is
+    refused before any call (checked on the CPU; the size, layout and element checks need device
+    tensors and are covered by the GPU tests)."""
+    torch = pytest.importorskip("torch")
+    N, K, M = 128, 256, 1
+    w = torch.zeros(woq.woq_packed_bytes(4, N, K), dtype=torch.uint8)
+    x = torch.zeros((M, K), dtype=torch.bfloat16)
+    y = torch.zeros((M, N), dtype=torch.float32)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        woq.woq_w4a8_linear_bf16(w, x, N, K, y, ws)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        woq.woq_act_quant_int8(x, torch.zeros((M, K), dtype=torch.int8), torch.zeros((M,)))
+    with pytest.raises(ValueError, match="2-D"):
+        woq.woq_w4a8_linear_bf16(w, x.reshape(-1), N, K, y, ws)

@@ -345,6 +345,33 @@ def test_max_k_bounds():
     assert e.value.status == woq.WOQ_ERR_SHAPE
 
 
+def test_binding_refuses_bad_tensors_before_any_launch():
+    """Undersized, non-contiguous or wrongly typed tensors are refused by the Python entries
+    (the library takes bare pointers without sizes); nothing is launched, y keeps its guards."""
+    bits, M, N, K = 4, 2, 256, 256
+    w, s = make_weights(bits, N, K, seed=3)
+    wdev = pack_host(bits, to_numpy_u8(w), to_numpy_u16(s), N, K)
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device=DEV)
+    out = Guarded(M, N)
+    ws = Workspace(bits, M, N, K)
+    small_y = out.buf[GUARD: GUARD + M * N - 1]
+    with pytest.raises(ValueError, match="elements"):
+        woq.woq_w4a8_linear_bf16(wdev, x, N, K, small_y, ws.ws)
+    with pytest.raises(ValueError, match="elements"):
+        woq.woq_w4a8_linear_bf16(wdev, torch.zeros((M, K - 8), dtype=torch.bfloat16, device=DEV), N, K, out.y, ws.ws)
+    with pytest.raises(ValueError, match="contiguous"):
+        woq.woq_w4a8_linear_bf16(wdev, torch.zeros((K, M), dtype=torch.bfloat16, device=DEV).t(), N, K, out.y, ws.ws)
+    with pytest.raises(ValueError, match="byte elements"):
+        woq.woq_w4a8_linear_bf16(wdev, x.float(), N, K, out.y, ws.ws)
+    q = torch.zeros((M, K), dtype=torch.int8, device=DEV)
+    with pytest.raises(ValueError, match="elements"):
+        woq.woq_w4a8_gemv(wdev, q, torch.zeros((M - 1,), device=DEV), N, K, out.y, ws.ws)
+    torch.cuda.synchronize()
+    out.check_guards()
+    assert (out.y.cpu().numpy() == np.float32(SENT)).all()
+    ws.check()
+
+
 def test_header_mismatch_sets_status_and_leaves_y():
     bits, M, N, K = 4, 1, 256, 256
     w, s = make_weights(bits, N, K, seed=1)

@@ -93,9 +93,31 @@ def _check(status: int, what: str) -> None:
         raise WoqError(status, what)
 
 
-def _dptr(t):
-    """Device pointer of a tensor (None -> NULL)."""
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _dptr(t, name: str = "tensor", itemsize: int = 0, numel: int = -1):
+    """Device pointer of a tensor (None -> NULL).  The C entries take bare pointers (most with
+    no size), so the tensor is checked here: a contiguous CUDA tensor on the current device,
+    elements of itemsize bytes (when given) and at least numel of them (when given)."""
+    if t is None:
+        return None
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    import torch
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name}: tensor is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if itemsize and t.element_size() != itemsize:
+        raise ValueError(f"{name}: expected {itemsize}-byte elements, got {t.dtype}")
+    if numel >= 0 and t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, the call needs {numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _rows(t, name: str) -> int:
+    """Row count M of a 2-D activation tensor."""
+    if t is None or t.dim() != 2:
+        raise ValueError(f"{name}: expected a 2-D [M, K] tensor")
+    return t.shape[0]
 
 
 def _nbytes(t) -> int:
@@ -167,14 +189,15 @@ def woq_unpack(bits: int, packed: np.ndarray, N: int, K: int):
 
 def woq_pack_device(bits: int, q_dev, scales_dev, N: int, K: int, dst_dev, stream=None) -> None:
     """Device pack into dst_dev (uint8 tensor of woq_packed_bytes(bits, N, K) bytes)."""
-    _check(lib.woq_pack_device(bits, _dptr(q_dev), _dptr(scales_dev), N, K, _dptr(dst_dev), _nbytes(dst_dev),
-                               _stream(stream)), "woq_pack_device")
+    row = K // 2 if bits == 4 else K // 4 * 3
+    _check(lib.woq_pack_device(bits, _dptr(q_dev, "q_dev", 1, N * row), _dptr(scales_dev, "scales_dev", 2, N * (K // GROUP)),
+                               N, K, _dptr(dst_dev, "dst_dev", 1), _nbytes(dst_dev), _stream(stream)), "woq_pack_device")
 
 
 def woq_relayout_inplace(bits: int, buf, N: int, K: int, stream=None) -> None:
     """In-place relayout of buf (uint8 device tensor of woq_packed_bytes(bits, N, K)
     bytes): canonical weights from byte 256 on, then the fp16 scales; packed on return."""
-    _check(lib.woq_relayout_inplace(bits, _dptr(buf), _nbytes(buf), N, K, _stream(stream)),
+    _check(lib.woq_relayout_inplace(bits, _dptr(buf, "buf", 1), _nbytes(buf), N, K, _stream(stream)),
            "woq_relayout_inplace")
 
 
@@ -191,12 +214,12 @@ def canonical_into_buffer(bits: int, q_dev, scales_dev, buf) -> None:
 # ----------------------------------------------------------------------------- workspace
 
 def woq_workspace_init(ws, stream=None) -> None:
-    _check(lib.woq_workspace_init(_dptr(ws), _nbytes(ws), _stream(stream)), "woq_workspace_init")
+    _check(lib.woq_workspace_init(_dptr(ws, "ws", 1), _nbytes(ws), _stream(stream)), "woq_workspace_init")
 
 
 def woq_read_status(ws, clear: bool = False, stream=None) -> int:
     v = ctypes.c_uint32(0)
-    _check(lib.woq_read_status(_dptr(ws), _nbytes(ws), int(clear), ctypes.byref(v), _stream(stream)),
+    _check(lib.woq_read_status(_dptr(ws, "ws", 1), _nbytes(ws), int(clear), ctypes.byref(v), _stream(stream)),
            "woq_read_status")
     return int(v.value)
 
@@ -205,15 +228,16 @@ def woq_read_status(ws, clear: bool = False, stream=None) -> int:
 
 def woq_act_quant_int8(x_bf16, q, ascale, stream=None) -> None:
     """x_bf16 [M, K] bf16 -> q [M, K] int8, ascale [M] fp32 (device tensors)."""
-    M, K = x_bf16.shape
-    _check(lib.woq_act_quant_int8(_dptr(x_bf16), M, K, _dptr(q), _dptr(ascale), _stream(stream)),
-           "woq_act_quant_int8")
+    M = _rows(x_bf16, "x_bf16")
+    K = x_bf16.shape[1]
+    _check(lib.woq_act_quant_int8(_dptr(x_bf16, "x_bf16", 2), M, K, _dptr(q, "q", 1, M * K),
+                                  _dptr(ascale, "ascale", 4, M), _stream(stream)), "woq_act_quant_int8")
 
 
 def _gemv(fn, name, wpacked, q, ascale, N, K, y, ws, stream):
-    M = q.shape[0]
-    _check(fn(_dptr(wpacked), _nbytes(wpacked), _dptr(q), _dptr(ascale), M, N, K, _dptr(y), _dptr(ws), _nbytes(ws),
-              _stream(stream)), name)
+    M = _rows(q, "q")
+    _check(fn(_dptr(wpacked, "wpacked", 1), _nbytes(wpacked), _dptr(q, "q", 1, M * K), _dptr(ascale, "ascale", 4, M),
+              M, N, K, _dptr(y, "y", 4, M * N), _dptr(ws, "ws", 1), _nbytes(ws), _stream(stream)), name)
 
 
 def woq_w4a8_gemv(wpacked, q, ascale, N: int, K: int, y, ws, stream=None) -> None:
@@ -225,9 +249,9 @@ def woq_w6a8_gemv(wpacked, q, ascale, N: int, K: int, y, ws, stream=None) -> Non
 
 
 def _linear(fn, name, wpacked, x_bf16, N, K, y, ws, stream):
-    M = x_bf16.shape[0]
-    _check(fn(_dptr(wpacked), _nbytes(wpacked), _dptr(x_bf16), M, N, K, _dptr(y), _dptr(ws), _nbytes(ws),
-              _stream(stream)), name)
+    M = _rows(x_bf16, "x_bf16")
+    _check(fn(_dptr(wpacked, "wpacked", 1), _nbytes(wpacked), _dptr(x_bf16, "x_bf16", 2, M * K), M, N, K,
+              _dptr(y, "y", 4, M * N), _dptr(ws, "ws", 1), _nbytes(ws), _stream(stream)), name)
 
 
 def woq_w4a8_linear_bf16(wpacked, x_bf16, N: int, K: int, y, ws, stream=None) -> None:
@@ -239,9 +263,10 @@ def woq_w6a8_linear_bf16(wpacked, x_bf16, N: int, K: int, y, ws, stream=None) ->
 
 
 def _linear_rmsnorm(fn, name, wpacked, x_bf16, gamma_bf16, eps, N, K, y, ws, stream):
-    M = x_bf16.shape[0]
-    _check(fn(_dptr(wpacked), _nbytes(wpacked), _dptr(x_bf16), _dptr(gamma_bf16), float(eps), M, N, K, _dptr(y),
-              _dptr(ws), _nbytes(ws), _stream(stream)), name)
+    M = _rows(x_bf16, "x_bf16")
+    _check(fn(_dptr(wpacked, "wpacked", 1), _nbytes(wpacked), _dptr(x_bf16, "x_bf16", 2, M * K),
+              _dptr(gamma_bf16, "gamma_bf16", 2, K), float(eps), M, N, K, _dptr(y, "y", 4, M * N),
+              _dptr(ws, "ws", 1), _nbytes(ws), _stream(stream)), name)
 
 
 def woq_w4a8_linear_rmsnorm_bf16(wpacked, x_bf16, gamma_bf16, eps: float, N: int, K: int, y, ws, stream=None) -> None:
@@ -256,9 +281,9 @@ def woq_w6a8_linear_rmsnorm_bf16(wpacked, x_bf16, gamma_bf16, eps: float, N: int
 
 
 def _linear_swiglu(fn, name, wpacked, gate_up, N, K, y, ws, stream):
-    M = gate_up.shape[0]
-    _check(fn(_dptr(wpacked), _nbytes(wpacked), _dptr(gate_up), M, N, K, _dptr(y), _dptr(ws), _nbytes(ws),
-              _stream(stream)), name)
+    M = _rows(gate_up, "gate_up")
+    _check(fn(_dptr(wpacked, "wpacked", 1), _nbytes(wpacked), _dptr(gate_up, "gate_up", 4, M * 2 * K), M, N, K,
+              _dptr(y, "y", 4, M * N), _dptr(ws, "ws", 1), _nbytes(ws), _stream(stream)), name)
 
 
 def woq_w4a8_linear_swiglu_f32(wpacked, gate_up, N: int, K: int, y, ws, stream=None) -> None:
@@ -271,29 +296,34 @@ def woq_w6a8_linear_swiglu_f32(wpacked, gate_up, N: int, K: int, y, ws, stream=N
 
 
 def woq_rmsnorm_act_quant_int8(x_bf16, gamma_bf16, eps: float, q, ascale, stream=None) -> None:
-    M, K = x_bf16.shape
-    _check(lib.woq_rmsnorm_act_quant_int8(_dptr(x_bf16), _dptr(gamma_bf16), float(eps), M, K, _dptr(q), _dptr(ascale),
+    M = _rows(x_bf16, "x_bf16")
+    K = x_bf16.shape[1]
+    _check(lib.woq_rmsnorm_act_quant_int8(_dptr(x_bf16, "x_bf16", 2), _dptr(gamma_bf16, "gamma_bf16", 2, K), float(eps),
+                                          M, K, _dptr(q, "q", 1, M * K), _dptr(ascale, "ascale", 4, M),
                                           _stream(stream)), "woq_rmsnorm_act_quant_int8")
 
 
 def woq_swiglu_act_quant_int8(gate_up, q, ascale, stream=None) -> None:
-    M, K2 = gate_up.shape
-    _check(lib.woq_swiglu_act_quant_int8(_dptr(gate_up), M, K2 // 2, _dptr(q), _dptr(ascale), _stream(stream)),
-           "woq_swiglu_act_quant_int8")
+    M = _rows(gate_up, "gate_up")
+    K = gate_up.shape[1] // 2
+    _check(lib.woq_swiglu_act_quant_int8(_dptr(gate_up, "gate_up", 4), M, K, _dptr(q, "q", 1, M * K),
+                                         _dptr(ascale, "ascale", 4, M), _stream(stream)), "woq_swiglu_act_quant_int8")
 
 
 def woq_w4a8_linear_bf16_noalloc(wpacked, x_bf16, N: int, K: int, y, stream=None) -> None:
     """woq_w4a8_linear_bf16 for callers that cannot allocate a workspace (the library's own
     2 MiB scratch is used; calls that overlap on the GPU race)."""
-    M = x_bf16.shape[0]
-    _check(lib.woq_w4a8_linear_bf16_noalloc(_dptr(wpacked), _nbytes(wpacked), _dptr(x_bf16), M, N, K, _dptr(y),
+    M = _rows(x_bf16, "x_bf16")
+    _check(lib.woq_w4a8_linear_bf16_noalloc(_dptr(wpacked, "wpacked", 1), _nbytes(wpacked),
+                                            _dptr(x_bf16, "x_bf16", 2, M * K), M, N, K, _dptr(y, "y", 4, M * N),
                                             _stream(stream)), "woq_w4a8_linear_bf16_noalloc")
 
 
 def woq_debug_group_dots(bits: int, wpacked, q, N: int, K: int, dots, stream=None) -> None:
-    M = q.shape[0]
-    _check(lib.woq_debug_group_dots(bits, _dptr(wpacked), _nbytes(wpacked), _dptr(q), M, N, K, _dptr(dots),
-                                    _stream(stream)), "woq_debug_group_dots")
+    M = _rows(q, "q")
+    _check(lib.woq_debug_group_dots(bits, _dptr(wpacked, "wpacked", 1), _nbytes(wpacked), _dptr(q, "q", 1, M * K), M, N,
+                                    K, _dptr(dots, "dots", 4, M * N * (K // GROUP)), _stream(stream)),
+           "woq_debug_group_dots")
 
 
 def woq_tune_override(ctas_per_sm: int = 0, stages: int = 0, prefetch_kb: int = -1) -> None:
