@@ -197,7 +197,8 @@ WOQ_API int woq_w6a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_
  * exactly as woq_act_quant_int8 does, then runs the GEMV.  Bit-identical to
  * woq_act_quant_int8 followed by woq_w?a8_gemv.  Same arguments as the GEMV,
  * with x_bf16 (device bf16 [M][K]) in place of q and ascale; K <= woq_max_k(bits, M, 1)
- * (x is staged as bf16 in shared memory).
+ * (shared memory keeps room for x as bf16; rows that fit registers are read from
+ * global memory straight into them, longer rows are copied in).
  * --------------------------------------------------------------------------- */
 WOQ_API int woq_w4a8_linear_bf16(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N, int K, float* y,
                          void* ws, size_t ws_bytes, woq_stream_t stream);
