@@ -275,7 +275,9 @@ WOQ_API int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_b
 
 /* ---------------------------------------------------------------------------
  * Tuning: override the launch table for the following GEMV / linear launches
- * of this process.  ctas_per_sm in {1, 2} (0 = table), stages in [2, 8]
+ * of this process.  ctas_per_sm in {1, 2} (0 = table; one CTA fits an SM, so 2
+ * runs the grid in two waves, and the SwiGLU entries, whose grid-wide step needs
+ * every CTA resident, keep one per SM), stages in [2, 8]
  * (0 = table), prefetch_kb = weight bytes per CTA kept in flight into L2
  * beyond the shared-memory ring, in KiB (-1 = table, 0 = none).  Not
  * thread-safe; meant for benchmark sweeps.  WOQ_ERR_SHAPE for values out of

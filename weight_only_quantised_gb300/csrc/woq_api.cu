@@ -119,7 +119,7 @@ int smem_bytes_for(int bits, int M, int K, bool fused, int stages) {
 // reads: 27B step at M = 1 2.33 ms, 2.40-2.41 ms with four to seven stages everywhere.
 static constexpr int kRingBudget = (233472 - 2 * 1024) / 2;
 
-LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
+LaunchConfig choose_config(int bits, int M, int N, int K, bool fused, bool resident_grid) {
   LaunchConfig cfg = {0, 0, 0, 0, 0};
   const int sms = sm_count();
   const int smem_max = max_dynamic_smem();
@@ -129,7 +129,9 @@ LaunchConfig choose_config(int bits, int M, int N, int K, bool fused) {
   const long long NB = T * G;
   if (NB <= 0) return cfg;
   int cps = g_override_cps.load(std::memory_order_relaxed);
-  if (cps <= 0) cps = 1;
+  // one CTA per SM is always resident (a CTA fits an SM alone or the launch fails); a second
+  // one never is at 112 registers, so a grid-wide step would wait for a wave that cannot start
+  if (cps <= 0 || resident_grid) cps = 1;
   int stages = g_override_stages.load(std::memory_order_relaxed);
   if (stages > 0) {
     const int budget = cps == 1 ? smem_max : kRingBudget;
@@ -348,7 +350,7 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   if (fused ? !aligned(x, 16) : (!aligned(q, 16) || !aligned(ascale, 4))) return WOQ_ERR_ALIGN;
   if (pro == kern::kProRms && !aligned(gamma, 16)) return WOQ_ERR_ALIGN;
   if (wpacked_bytes < packed_bytes(bits, N, K)) return WOQ_ERR_LAYOUT;
-  const LaunchConfig cfg = choose_config(bits, M, N, K, fused);
+  const LaunchConfig cfg = choose_config(bits, M, N, K, fused, pro == kern::kProSwiglu);
   if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
   const WorkspaceLayout wl = workspace_layout(M, N, K, cfg.ctas);
   if (ws_bytes < wl.total || cfg.ctas > max_ctas_for_workspace()) return WOQ_ERR_WORKSPACE;

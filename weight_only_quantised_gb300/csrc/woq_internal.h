@@ -36,7 +36,9 @@ int sm_count();                       // SMs of the current device (cached per d
 int max_dynamic_smem();               // opt-in shared memory per block of the current device
 int choose_consumer(int bits, int M);  // kern::Consumer the launch table picks for (bits, M)
 int smem_bytes_for(int bits, int M, int K, bool fused, int stages);
-LaunchConfig choose_config(int bits, int M, int N, int K, bool fused);
+// resident_grid: the launch has a grid-wide step (the SwiGLU prologue), so its CTAs must all be
+// resident at once: at most one per SM, whatever the tuning override says
+LaunchConfig choose_config(int bits, int M, int N, int K, bool fused, bool resident_grid = false);
 WorkspaceLayout workspace_layout(int M, int N, int K, int ctas);
 
 // Kernel launchers (woq_gemv.cu); return a cudaError_t.
