@@ -431,16 +431,18 @@ struct StageCursor {
 };
 
 // Activation prologue of the fused entry, run by the consumer warps on the bf16 x
-// that one bulk copy placed at act[0, 2 M K): per-row amax, scale = amax / 127, and
-// q = rne(x / scale) written in place, row m at act + m qs (qs = K or K + 16 <= 2K, so
-// the q byte of value e overwrites only x bytes of values with index <= e).
+// that one bulk copy placed at act[0, 2 M K) (or, with X_GLOBAL, on x in global
+// memory): per-row amax, scale = amax / 127, and q = rne(x / scale) written to
+// act + m qs for row m (qs = K or K + 16 <= 2K, so in place the q byte of value e
+// overwrites only x bytes of values with index <= e).
 //
 // The amax covers the whole row; q is only formed for k in [klo1, khi1) and [klo2, khi2),
 // the groups this CTA's blocks read (the rest of the tile is never looked at).
 //
-// Rows with K <= kConsumers * 8 * (kRegVecs / M) are read once into registers; the
-// barrier after the amax pass then guarantees that every x value has been read
-// before any q byte is written.  Longer rows are quantised in rounds, each read in
+// Rows with K <= kConsumers * 8 * (kRegVecs / M) are read once into registers (from
+// shared memory, or straight from global memory with X_GLOBAL); the barrier after the
+// amax pass then guarantees that every x value has been read before any q byte is
+// written.  Longer rows are quantised in rounds, each read in
 // full before any thread of the round writes (the amax pass has read everything
 // before the first write, so skipped rounds need no reads).  Every vector is stored
 // as the fast route gives it; one warp vote afterwards sends the rare vectors with a
