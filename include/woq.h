@@ -4,7 +4,7 @@
  * The op ("Doubling LLM token rates in ComfyUI", blog.comfy.org, sections
  * "What is the bottleneck?" and "Optimizing the Linear Kernel"):
  *
- *     y[M x N] = dequant(W[N x K]) . quant8(x[M x K]),   M = 1 .. 4
+ *     y[M x N] = dequant(W[N x K]) . quant8(x[M x K]),   M = 1 .. 8 (int4), 1 .. 4 (int6)
  *
  * W holds 4-bit (W4A8) or 6-bit (W6A8) signed weights with one fp16 scale per
  * row and group of 128 consecutive k; x is quantised per row to int8 with
@@ -20,8 +20,9 @@
  *     global memory of the current device.  The caller owns every buffer; the
  *     library allocates no memory (device or pinned) in any entry point.
  *   - Device entry points are asynchronous on the given stream (NULL = the
- *     legacy default stream).  Launch failures return WOQ_ERR_CUDA; a fault in
- *     a kernel surfaces at the caller's next synchronisation.
+ *     legacy default stream).  Launch failures return WOQ_ERR_CUDA (the CUDA code
+ *     is kept for woq_last_cuda_error); a fault in a kernel surfaces at the
+ *     caller's next synchronisation.
  *   - Device buffers must be 16-byte aligned, except y, ascale and dots (4 bytes).
  *   - Empty shapes are valid: M == 0 or N == 0 launches nothing and returns
  *     WOQ_OK; K == 0 (no groups) zero-fills y.
@@ -32,9 +33,10 @@
  *   - Kernels are launched with programmatic dependent launch: a woq kernel may
  *     start streaming weights while the previous kernel in the stream is still
  *     running, and waits for it before it reads activations or touches y or the
- *     workspace.  Weights must therefore not be written by the kernel that
- *     directly precedes a woq launch in the stream if that kernel is itself a
- *     woq GEMV/linear launch (woq kernels never write weights).
+ *     workspace.  The weights (and their header) are read before that wait, so
+ *     a kernel that writes a launch's weights must not let dependents start
+ *     early (griddepcontrol.launch_dependents): ordinary kernels, PyTorch's and
+ *     the woq packers included, do not; woq kernels that do never write weights.
  */
 #ifndef WOQ_H
 #define WOQ_H
