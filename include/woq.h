@@ -296,6 +296,26 @@ WOQ_API int woq_last_cuda_error(void);
 /* cudaGetErrorName of a code returned by woq_last_cuda_error (static string). */
 WOQ_API const char* woq_cuda_error_name(int code);
 
+/* The launch table's choice for one GEMV / linear launch, worked out on the host
+ * without launching anything.
+ *   entry: 0 = int8 GEMV (woq_w?a8_gemv), 1 = bf16 or RMSNorm linear, 2 = SwiGLU
+ *   linear; sms, smem_max: the device to plan for (SM count, opt-in shared memory
+ *   per block in bytes), 0 for either = the current device's value.  The tuning
+ *   overrides in force apply.  out (host) is filled on WOQ_OK.
+ *   Errors: WOQ_ERR_NULL (out NULL); WOQ_ERR_SHAPE (1 <= M <= woq_max_m() for int4
+ *   or 4 for int6, N >= 1, K >= 128, K % 128 == 0, M * K <= 98304 and entry in
+ *   0..2 not met, or no ring of two stages fits smem_max); WOQ_ERR_CUDA (the
+ *   current device could not be queried). */
+typedef struct {
+  int ctas;            /* grid: one CTA per SM (two with the tuning override), fewer
+                          when the matrix has fewer four-block stages than that */
+  int stages;          /* shared-memory ring stages (four blocks each) */
+  int prefetch_stages; /* stages kept in flight into L2 beyond the ring */
+  int smem_bytes;      /* dynamic shared memory per CTA */
+  int consumer;        /* 0 = dp4a, 1 = f16 tensor-core MMA */
+} woq_launch_plan;
+WOQ_API int woq_plan_launch(int bits, int M, int N, int K, int entry, int sms, int smem_max, woq_launch_plan* out);
+
 /* Tuning: which consumer the following int4 GEMV / linear launches of this process
  * use: 0 = launch table (dp4a), 1 = dp4a, 2 = f16 tensor-core MMA.  Both form the
  * same exact per-group integer dots; outputs agree within the GEMV tolerance.

@@ -326,6 +326,28 @@ def woq_debug_group_dots(bits: int, wpacked, q, N: int, K: int, dots, stream=Non
            "woq_debug_group_dots")
 
 
+class LaunchPlan(ctypes.Structure):
+    """woq_launch_plan of include/woq.h."""
+    _fields_ = [("ctas", ctypes.c_int), ("stages", ctypes.c_int), ("prefetch_stages", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("consumer", ctypes.c_int)]
+
+
+lib.woq_plan_launch.argtypes = [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(LaunchPlan)]
+lib.woq_plan_launch.restype = _I
+
+PLAN_INT8, PLAN_BF16, PLAN_SWIGLU = 0, 1, 2  # entry kinds of woq_plan_launch
+
+
+def woq_plan_launch(bits: int, M: int, N: int, K: int, entry: int = PLAN_BF16, sms: int = 0,
+                    smem_max: int = 0) -> dict:
+    """The launch table's choice (grid, ring stages, L2 prefetch stages, shared memory, consumer)
+    for one launch, on the current device or on one with sms SMs and smem_max bytes of opt-in
+    shared memory per block; nothing is launched."""
+    plan = LaunchPlan()
+    _check(lib.woq_plan_launch(bits, M, N, K, entry, sms, smem_max, ctypes.byref(plan)), "woq_plan_launch")
+    return {name: getattr(plan, name) for name, _ in LaunchPlan._fields_}
+
+
 def woq_tune_override(ctas_per_sm: int = 0, stages: int = 0, prefetch_kb: int = -1) -> None:
     _check(lib.woq_tune_override(ctas_per_sm, stages, prefetch_kb), "woq_tune_override")
 

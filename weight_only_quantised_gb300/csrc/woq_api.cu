@@ -120,9 +120,11 @@ int smem_bytes_for(int bits, int M, int K, bool fused, int stages) {
 static constexpr int kRingBudget = (233472 - 2 * 1024) / 2;
 
 LaunchConfig choose_config(int bits, int M, int N, int K, bool fused, bool resident_grid) {
+  return choose_config_for(sm_count(), max_dynamic_smem(), bits, M, N, K, fused, resident_grid);
+}
+
+LaunchConfig choose_config_for(int sms, int smem_max, int bits, int M, int N, int K, bool fused, bool resident_grid) {
   LaunchConfig cfg = {0, 0, 0, 0, 0};
-  const int sms = sm_count();
-  const int smem_max = max_dynamic_smem();
   if (sms <= 0 || smem_max <= 0) return cfg;
   const long long T = (N + kTileRows - 1) / kTileRows;
   const long long G = K / kGroup;
@@ -132,15 +134,16 @@ LaunchConfig choose_config(int bits, int M, int N, int K, bool fused, bool resid
   // one CTA per SM is always resident (a CTA fits an SM alone or the launch fails); a second
   // one never is at 112 registers, so a grid-wide step would wait for a wave that cannot start
   if (cps <= 0 || resident_grid) cps = 1;
+  const int ring_budget = kRingBudget < smem_max ? kRingBudget : smem_max;
   int stages = g_override_stages.load(std::memory_order_relaxed);
   if (stages > 0) {
-    const int budget = cps == 1 ? smem_max : kRingBudget;
+    const int budget = cps == 1 ? smem_max : ring_budget;
     while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > budget) --stages;
   } else {
     // up to four stages within the ring budget, else the largest ring that fits.  Two rows take
     // four stages wherever they fit (within the budget their 2 M K byte activations leave some
     // linears only two stages): 27B step at M = 2 2.722 ms against 2.760 ms.
-    const int budget = M == 2 ? smem_max : kRingBudget;
+    const int budget = M == 2 ? smem_max : ring_budget;
     stages = 4;
     while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > budget) --stages;
     if (stages < 2 && cps == 1) {
@@ -228,6 +231,26 @@ int woq_tune_override(int ctas_per_sm, int stages, int prefetch_kb) {
 int woq_tune_path(int path) {
   if (path < 0 || path > 2) return WOQ_ERR_SHAPE;
   g_override_path.store(path);
+  return WOQ_OK;
+}
+
+int woq_plan_launch(int bits, int M, int N, int K, int entry, int sms, int smem_max, woq_launch_plan* out) {
+  if (!out) return WOQ_ERR_NULL;
+  if ((bits != 4 && bits != 6) || M < 1 || M > max_m_for(bits) || N < 1 || K < kGroup || K % kGroup ||
+      (long)M * K > kMaxMK || entry < 0 || entry > 2 || sms < 0 || smem_max < 0)
+    return WOQ_ERR_SHAPE;
+  if (sms == 0) sms = sm_count();
+  if (smem_max == 0) smem_max = max_dynamic_smem();
+  if (sms <= 0 || smem_max <= 0) return WOQ_ERR_CUDA;
+  const LaunchConfig cfg = choose_config_for(sms, smem_max, bits, M, N, K, entry != 0, entry == 2);
+  if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
+  const unsigned long long nb = (unsigned long long)((N + kTileRows - 1) / kTileRows) * (unsigned long long)(K / kGroup);
+  if ((nb + 1) * (unsigned long long)(cfg.ctas + 1) >= (1ull << 32)) return WOQ_ERR_SHAPE;
+  out->ctas = cfg.ctas;
+  out->stages = cfg.stages;
+  out->prefetch_stages = cfg.prefetch_stages;
+  out->smem_bytes = cfg.smem_bytes;
+  out->consumer = cfg.consumer;
   return WOQ_OK;
 }
 

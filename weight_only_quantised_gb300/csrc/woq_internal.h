@@ -39,6 +39,9 @@ int smem_bytes_for(int bits, int M, int K, bool fused, int stages);
 // resident_grid: the launch has a grid-wide step (the SwiGLU prologue), so its CTAs must all be
 // resident at once: at most one per SM, whatever the tuning override says
 LaunchConfig choose_config(int bits, int M, int N, int K, bool fused, bool resident_grid = false);
+// The same choice for a device with sms SMs and smem_max bytes of opt-in shared memory per block
+// (ctas == 0 when nothing fits).
+LaunchConfig choose_config_for(int sms, int smem_max, int bits, int M, int N, int K, bool fused, bool resident_grid);
 WorkspaceLayout workspace_layout(int M, int N, int K, int ctas);
 
 // Kernel launchers (woq_gemv.cu); return a cudaError_t.
