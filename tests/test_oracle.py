@@ -359,6 +359,47 @@ def test_rmsnorm_matches_fp64_and_its_invariants():
     assert (oracle.rmsnorm(c, np.full(256, 0x3F80, np.uint16), 0.0) == 0xBF80).all()  # -1.0
 
 
+def test_rmsnorm_eps_enters_under_the_square_root():
+    """eps is added to the mean of squares, under the square root, and nowhere else.
+    Rows of +-1 have mean of squares exactly 1: eps = 3 gives r = 1/sqrt(4) = 1/2 exactly, so
+    h = +-gamma / 2 (a dropped eps gives +-gamma, an eps added after the square root
+    +-gamma / 4).  The same at another scale: x = +-2^-10 (mean 2^-20) with eps = 3 2^-20 gives
+    r = 2^9 and h = +-gamma / 2 again.  eps = 1 gives h within one bf16 step of
+    +-gamma / sqrt(2)."""
+    import torch
+    rng = np.random.default_rng(8)
+    M, K = 3, 1024
+    sign = rng.random((M, K)) < 0.5
+    gv = (1.0 + rng.standard_normal(K)).astype(np.float32)
+    gamma = _bf16_bits(torch.from_numpy(gv))
+    gval = _bf16_value(gamma)
+    for xmag, eps, factor in [(1.0, 3.0, 0.5), (2.0 ** -10, 3.0 * 2.0 ** -20, 0.5), (1.0, 0.0, 1.0)]:
+        x = _bf16_bits(torch.from_numpy(np.where(sign, -xmag, xmag).astype(np.float32)))
+        h = _bf16_value(oracle.rmsnorm(x, gamma, eps))
+        assert np.array_equal(h, np.where(sign, -1.0, 1.0) * gval * factor), (xmag, eps)
+    x = _bf16_bits(torch.from_numpy(np.where(sign, -1.0, 1.0).astype(np.float32)))
+    ref = np.where(sign, -1.0, 1.0) * gval / np.sqrt(2.0)
+    h = _bf16_value(oracle.rmsnorm(x, gamma, 1.0))
+    assert (np.abs(h - ref) <= np.abs(ref) * 2.0 ** -7).all()
+
+
+def test_rmsnorm_matches_fp64_where_eps_is_large():
+    """Small activations (mean of squares about 1e-4) with eps from 1e-5 to 1e-2: eps changes r
+    by up to a factor of ten, and h stays within one bf16 step of the fp64 RMSNorm."""
+    import torch
+    rng = np.random.default_rng(9)
+    M, K = 4, 4096
+    x = torch.from_numpy((rng.standard_normal((M, K)) * 0.01).astype(np.float32))
+    xb = _bf16_bits(x)
+    gamma = _bf16_bits(torch.from_numpy((1.0 + 0.1 * rng.standard_normal(K)).astype(np.float32)))
+    xv, gv = _bf16_value(xb), _bf16_value(gamma)
+    for eps in (1e-5, 1e-4, 1e-3, 1e-2):
+        e32 = float(np.float32(eps))
+        ref = xv / np.sqrt((xv ** 2).mean(axis=1, keepdims=True) + e32) * gv
+        h = _bf16_value(oracle.rmsnorm(xb, gamma, eps))
+        assert (np.abs(h - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30).all(), eps
+
+
 def test_fused_linear_oracles_compose_the_steps():
     rng = np.random.default_rng(7)
     N, K, M = 64, 256, 2
