@@ -153,7 +153,8 @@ WOQ_API int woq_relayout_inplace(int bits, void* buf, size_t buf_bytes, int N, i
  * before first use (woq_workspace_init); every successful launch leaves its
  * synchronisation words zero again (after a WOQ_DEVERR_TIMEOUT, zero-fill it
  * again).  Its last M * K * 2 bytes are scratch rows of the SwiGLU entries,
- * overwritten by every such launch.  One workspace must
+ * overwritten by every such launch (the other entries do not touch them, and
+ * accept a workspace without them).  One workspace must
  * not be used by two launches that can run at the same time.  Its size depends
  * on the current device's SM count.
  * --------------------------------------------------------------------------- */
@@ -254,18 +255,50 @@ WOQ_API int woq_swiglu_act_quant_int8(const float* gate_up, int M, int K, int8_t
  * with a fixed memory budget where a cudaMalloc could synchronise or fail).
  *   Same inputs and outputs as woq_w4a8_linear_bf16, without a workspace: its
  *   scratch is a 2 MiB array built into the library, present on every GPU that
- *   loads it until the process exits (enough for M <= 4 with grids of up to 255
- *   CTAs, and for larger M with fewer CTAs; a shape whose launch would need more
- *   returns WOQ_ERR_WORKSPACE).
+ *   loads it until the process exits.  A launch needs 256 bytes plus 2048 * M
+ *   bytes per CTA (grids of up to 255 CTAs at M = 4, 1023 / M CTAs in general; on
+ *   a 152-SM GPU every shape with M <= 6); a shape whose launch would need more
+ *   returns WOQ_ERR_WORKSPACE before anything is enqueued.
  *   The first call on each device looks up the array's device address (with that
- *   device current); make that first call before any stream capture.  Every call
- *   zeroes the part of the scratch it uses (an asynchronous memset on the stream)
- *   and then launches the linear; it allocates nothing.  All calls share the one
- *   array, so calls that can overlap on the GPU (different streams, or a woq
- *   linear/GEMV launch running at the same time) race and must be avoided.
+ *   device current) and keeps it for the life of the process; make that first call
+ *   before any stream capture.  A device reset (cudaDeviceReset) is not supported
+ *   afterwards.  Every call zeroes the split-tile words it uses (an asynchronous
+ *   memset on the stream) and then launches the linear; it allocates nothing.  The
+ *   array's status word is not zeroed: a device-side error (WOQ_DEVERR_*) stays in
+ *   it until woq_noalloc_read_status clears it, and with it y may be stale or
+ *   partly written.  All calls share the one array, so calls that can overlap on
+ *   the GPU (different streams, or a woq linear/GEMV launch running at the same
+ *   time) race and must be avoided.
  * --------------------------------------------------------------------------- */
 WOQ_API int woq_w4a8_linear_bf16_noalloc(const void* wpacked, size_t wpacked_bytes, const void* x_bf16, int M, int N,
                                          int K, float* y, woq_stream_t stream);
+
+/* Status word of woq_w4a8_linear_bf16_noalloc's built-in scratch on the current
+ * device, like woq_read_status: synchronises the stream, writes the WOQ_DEVERR_*
+ * bits of every allocation-free call since the last clear to *status_out (host)
+ * and, if clear != 0, zeroes them.  Errors: WOQ_ERR_NULL, WOQ_ERR_CUDA. */
+WOQ_API int woq_noalloc_read_status(int clear, uint32_t* status_out, woq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Next-linear prefetch hint (section "What is the bottleneck?": a decode step
+ * reads the weights of one linear after another, and the memory bus is only
+ * busy in bursts; section "Optimizing the Linear Kernel" counts the gaps
+ * between the bursts among the costs of a small kernel).
+ *   Tells the next GEMV / linear call made by this thread which linear will run
+ *   after it: next_wpacked (device, the packed weights of (bits, N, K), at least
+ *   woq_packed_bytes(bits, N, K) bytes).  That call, once its own weight stream has
+ *   been issued, brings into L2 the first budget_kb KiB (0 = 48) of the weights
+ *   each of the next launch's CTAs will stream first, planned as a launch of the
+ *   same entry kind and M.  The next launch then finds them in L2; every weight
+ *   byte is still read from HBM once.  A hint only: results are the same with or
+ *   without it, and a wrong hint only costs bandwidth.  Each GEMV / linear call
+ *   consumes the hint (launched or not); next_wpacked NULL clears it.  The hint is
+ *   per host thread; under stream capture it is baked into the captured launch.
+ *   Errors: WOQ_ERR_SHAPE (bits not 4 or 6, N < 0, K < 0, K % 128, budget_kb
+ *   outside [0, 65536]), WOQ_ERR_ALIGN, WOQ_ERR_LAYOUT (next_wpacked_bytes too small).
+ * --------------------------------------------------------------------------- */
+WOQ_API int woq_prefetch_next(const void* next_wpacked, size_t next_wpacked_bytes, int bits, int N, int K,
+                              int budget_kb);
 
 /* ---------------------------------------------------------------------------
  * Debug: the exact per-group integer dot products the GEMV scales.
@@ -315,6 +348,24 @@ typedef struct {
   int consumer;        /* 0 = dp4a, 1 = f16 tensor-core MMA */
 } woq_launch_plan;
 WOQ_API int woq_plan_launch(int bits, int M, int N, int K, int entry, int sms, int smem_max, woq_launch_plan* out);
+
+/* Tests of the bounded waits (section 8(b) of no page: the pages describe no failure
+ * handling; every wait of a woq kernel on another CTA is bounded so that a stuck CTA
+ * never hangs a shared GPU).  Injects one fault into the following launches of this
+ * process, made by CTA `cta` (a block index), and bounds the waits it makes run out by
+ * wait_limit_us microseconds (0 = the default, 2 s):
+ *   kind 1: GEMV / linear launches - that CTA never publishes its split-tile partial
+ *           sums; the combiner of such a tile gives up, sets WOQ_DEVERR_TIMEOUT and
+ *           leaves that tile's rows of y untouched;
+ *   kind 2: SwiGLU linears - that CTA never counts itself in at the row maxima; every
+ *           CTA gives up, sets WOQ_DEVERR_TIMEOUT and leaves y untouched;
+ *   kind 3: woq_relayout_inplace - that CTA leaves before the first grid barrier; the
+ *           others give up and the call returns WOQ_ERR_DEVICE (buffer contents undefined);
+ *   kind 0: no fault (the default).
+ * Nothing faults or waits without a bound; after kinds 1 and 2 the workspace must be
+ * zero-filled again (woq_workspace_init).  Not thread-safe; for tests only.
+ * WOQ_ERR_SHAPE for kind outside 0..3, cta < 0 or wait_limit_us outside [0, 2e6]. */
+WOQ_API int woq_tune_fault(int kind, int cta, int wait_limit_us);
 
 /* Tuning: which consumer the following int4 GEMV / linear launches of this process
  * use: 0 = launch table (dp4a), 1 = dp4a, 2 = f16 tensor-core MMA.  Both form the

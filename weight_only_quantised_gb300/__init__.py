@@ -61,8 +61,11 @@ _SIGS = {
     "woq_w6a8_linear_bf16": ([_P, _Z, _P, _I, _I, _I, _P, _P, _Z, _P], _I),
     "woq_debug_group_dots": ([_I, _P, _Z, _P, _I, _I, _I, _P, _P], _I),
     "woq_w4a8_linear_bf16_noalloc": ([_P, _Z, _P, _I, _I, _I, _P, _P], _I),
+    "woq_noalloc_read_status": ([_I, ctypes.POINTER(ctypes.c_uint32), _P], _I),
     "woq_tune_override": ([_I, _I, _I], _I),
     "woq_tune_path": ([_I], _I),
+    "woq_tune_fault": ([_I, _I, _I], _I),
+    "woq_prefetch_next": ([_P, _Z, _I, _I, _I, _I], _I),
     "woq_last_cuda_error": ([], _I),
     "woq_cuda_error_name": ([_I], ctypes.c_char_p),
     "woq_w4a8_linear_rmsnorm_bf16": ([_P, _Z, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _Z, _P], _I),
@@ -319,6 +322,13 @@ def woq_w4a8_linear_bf16_noalloc(wpacked, x_bf16, N: int, K: int, y, stream=None
                                             _stream(stream)), "woq_w4a8_linear_bf16_noalloc")
 
 
+def woq_noalloc_read_status(clear: bool = False, stream=None) -> int:
+    """Status word (WOQ_DEVERR_* bits) of the allocation-free linear's built-in scratch."""
+    v = ctypes.c_uint32(0)
+    _check(lib.woq_noalloc_read_status(int(clear), ctypes.byref(v), _stream(stream)), "woq_noalloc_read_status")
+    return int(v.value)
+
+
 def woq_debug_group_dots(bits: int, wpacked, q, N: int, K: int, dots, stream=None) -> None:
     M = _rows(q, "q")
     _check(lib.woq_debug_group_dots(bits, _dptr(wpacked, "wpacked", 1), _nbytes(wpacked), _dptr(q, "q", 1, M * K), M, N,
@@ -348,8 +358,23 @@ def woq_plan_launch(bits: int, M: int, N: int, K: int, entry: int = PLAN_BF16, s
     return {name: getattr(plan, name) for name, _ in LaunchPlan._fields_}
 
 
+def woq_prefetch_next(next_wpacked, bits: int, N: int, K: int, budget_kb: int = 0) -> None:
+    """Hint for the next GEMV / linear call of this thread: the linear that runs after it
+    (packed weights next_wpacked of (bits, N, K)); None clears the hint."""
+    if next_wpacked is None:
+        _check(lib.woq_prefetch_next(None, 0, bits, N, K, 0), "woq_prefetch_next")
+        return
+    _check(lib.woq_prefetch_next(_dptr(next_wpacked, "next_wpacked", 1), _nbytes(next_wpacked), bits, N, K, budget_kb),
+           "woq_prefetch_next")
+
+
 def woq_tune_override(ctas_per_sm: int = 0, stages: int = 0, prefetch_kb: int = -1) -> None:
     _check(lib.woq_tune_override(ctas_per_sm, stages, prefetch_kb), "woq_tune_override")
+
+
+def woq_tune_fault(kind: int = 0, cta: int = 0, wait_limit_us: int = 0) -> None:
+    """Tests of the bounded waits: inject one CTA's missing arrival (include/woq.h)."""
+    _check(lib.woq_tune_fault(kind, cta, wait_limit_us), "woq_tune_fault")
 
 
 def woq_tune_path(path: int = 0) -> None:

@@ -21,6 +21,15 @@ std::atomic<int> g_override_stages{0};
 std::atomic<int> g_override_prefetch_kb{-1};
 std::atomic<int> g_override_path{0};  // 0: table, else 1 + kern::Consumer
 std::atomic<int> g_launch_counter{0};  // numbers GEMV launches (trace builds key their stamps by it)
+// woq_tune_fault: a fault to inject (0 none, 1 split-tile publish, 2 SwiGLU arrival, 3 relayout
+// barrier arrival) by one CTA, and the bound of the waits it makes run out (0 = the default)
+std::atomic<int> g_fault_kind{0};
+std::atomic<int> g_fault_cta{0};
+std::atomic<long long> g_wait_ns{0};
+uint64_t wait_bound_ns() {
+  const long long v = g_wait_ns.load(std::memory_order_relaxed);
+  return v > 0 ? (uint64_t)v : dev::kWaitLimitNs;
+}
 
 // A failed CUDA call: remembered for woq_last_cuda_error (per thread) and cleared from the
 // runtime's error state, so that it does not surface again in the caller's next call.
@@ -190,6 +199,12 @@ WorkspaceLayout workspace_layout(int M, int N, int K, int ctas) {
 // workspace is sized for the largest grid the table or an override may pick
 static int max_ctas_for_workspace() { return 2 * sm_count(); }
 
+// Bytes of workspace a launch reads or writes: the status and synchronisation words and the
+// split-tile partials, plus the scratch rows for the SwiGLU prologue (the only one using them).
+static size_t workspace_need(int pro, const WorkspaceLayout& wl) {
+  return pro == kern::kProSwiglu ? wl.total : wl.h_offset;
+}
+
 }  // namespace woq
 
 using namespace woq;
@@ -225,6 +240,14 @@ int woq_tune_override(int ctas_per_sm, int stages, int prefetch_kb) {
   g_override_cps.store(ctas_per_sm);
   g_override_stages.store(stages);
   g_override_prefetch_kb.store(prefetch_kb);
+  return WOQ_OK;
+}
+
+int woq_tune_fault(int kind, int cta, int wait_limit_us) {
+  if (kind < 0 || kind > 3 || cta < 0 || wait_limit_us < 0 || wait_limit_us > 2000000) return WOQ_ERR_SHAPE;
+  g_fault_kind.store(kind);
+  g_fault_cta.store(cta);
+  g_wait_ns.store((long long)wait_limit_us * 1000);
   return WOQ_OK;
 }
 
@@ -317,7 +340,8 @@ int woq_relayout_inplace(int bits, void* buf, size_t buf_bytes, int N, int K, wo
     return cuda_result(e);
   }
   int too_large = 0;
-  cudaError_t e = launch_relayout(bits, buf, N, K, &too_large, (cudaStream_t)stream);
+  const int fault_cta = g_fault_kind.load(std::memory_order_relaxed) == 3 ? g_fault_cta.load(std::memory_order_relaxed) : -1;
+  cudaError_t e = launch_relayout(bits, buf, N, K, &too_large, (cudaStream_t)stream, wait_bound_ns(), fault_cta);
   if (too_large) return WOQ_ERR_SHAPE;
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
   uint32_t head[4] = {0u, 0u, 0u, 0u};
@@ -353,11 +377,47 @@ int woq_swiglu_act_quant_int8(const float* gate_up, int M, int K, int8_t* q, flo
   return cuda_result(launch_pro_act_quant(kern::kProSwiglu, gate_up, nullptr, 0.0f, M, K, q, ascale, (cudaStream_t)stream));
 }
 
+// The next-linear hint of this thread (woq_prefetch_next), consumed by its next GEMV / linear call.
+struct NextHint {
+  const void* w;
+  int bits, N, K, kb;
+};
+static thread_local NextHint t_next = {nullptr, 0, 0, 0, 0};
+static constexpr int kPrefetchNextKb = 48;  // default per-CTA prefetch of the next linear (27B step sweep: 32-64 best)
+
+// Fill the next-linear prefetch fields of p from a hint (none if the hint is empty or its
+// partition does not fit the 32-bit math); the next launch is planned like this one.
+static void plan_next_prefetch(GemvParams& p, const NextHint& h, int M, bool fused) {
+  p.nx_w = nullptr;
+  p.nx_NB = p.nx_C = p.nx_bb = p.nx_blocks = 0;
+  p.nx_div_c = FastDiv::make(1u);
+  p.nx_div_g = FastDiv::make(1u);
+  if (!h.w || h.N <= 0 || h.K <= 0) return;
+  const int mm = M <= max_m_for(h.bits) ? M : max_m_for(h.bits);
+  const LaunchConfig nc = choose_config(h.bits, mm, h.N, h.K, fused, false);
+  if (nc.ctas <= 0) return;
+  const unsigned long long T = (unsigned long long)((h.N + kTileRows - 1) / kTileRows), G = (unsigned long long)(h.K / kGroup);
+  const unsigned long long nb = T * G;
+  if ((nb + 1) * (unsigned long long)(nc.ctas + 1) >= (1ull << 32)) return;
+  const uint32_t bb = (uint32_t)block_bytes(h.bits);
+  const uint32_t blocks = (uint32_t)(((unsigned long long)(h.kb > 0 ? h.kb : kPrefetchNextKb) * 1024ull) / bb);
+  if (blocks == 0) return;
+  p.nx_w = static_cast<const uint8_t*>(h.w);
+  p.nx_NB = (uint32_t)nb;
+  p.nx_C = (uint32_t)nc.ctas;
+  p.nx_bb = bb;
+  p.nx_blocks = blocks;
+  p.nx_div_c = FastDiv::make((uint32_t)nc.ctas);
+  p.nx_div_g = FastDiv::make((uint32_t)G);
+}
+
 // pro: kern::Prologue.  x: bf16 [M][K] (bf16, RMSNorm) or fp32 [M][2K] (SwiGLU).
 static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes, const void* x, const int8_t* q,
                     const float* ascale, const uint16_t* gamma, float eps, int M, int N, int K, float* y, void* ws,
                     size_t ws_bytes, cudaStream_t stream) {
   const bool fused = pro != kern::kProInt8;
+  const NextHint next = t_next;  // every call consumes the hint, launched or not
+  t_next = NextHint{nullptr, 0, 0, 0, 0};
   if (M < 0 || M > max_m_for(bits) || N < 0 || K < 0 || K % kGroup || (long)M * K > kMaxMK) return WOQ_ERR_SHAPE;
   if (M == 0 || N == 0) return WOQ_OK;  // nothing to compute
   if (!y) return WOQ_ERR_NULL;
@@ -376,7 +436,7 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   const LaunchConfig cfg = choose_config(bits, M, N, K, fused, pro == kern::kProSwiglu);
   if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
   const WorkspaceLayout wl = workspace_layout(M, N, K, cfg.ctas);
-  if (ws_bytes < wl.total || cfg.ctas > max_ctas_for_workspace()) return WOQ_ERR_WORKSPACE;
+  if (ws_bytes < workspace_need(pro, wl) || cfg.ctas > max_ctas_for_workspace()) return WOQ_ERR_WORKSPACE;
   GemvParams p;
   p.w = static_cast<const uint8_t*>(wpacked);
   p.x = x;
@@ -389,8 +449,11 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   p.status = reinterpret_cast<uint32_t*>(wsb);
   p.parts = reinterpret_cast<unsigned long long*>(wsb + wl.parts_offset);
   p.sync = reinterpret_cast<uint32_t*>(wsb + kSyncOffset);
-  // the scratch rows are the last M K 2 bytes of the caller's workspace (16-byte aligned)
-  p.hbuf = reinterpret_cast<uint16_t*>(wsb + ((ws_bytes - (size_t)M * (size_t)K * 2) & ~(size_t)15));
+  // the scratch rows (SwiGLU prologue only) are the last M K 2 bytes of the caller's workspace
+  // (16-byte aligned; ws_bytes >= wl.total puts them at or after wl.h_offset)
+  p.hbuf = pro == kern::kProSwiglu
+               ? reinterpret_cast<uint16_t*>(wsb + ((ws_bytes - (size_t)M * (size_t)K * 2) & ~(size_t)15))
+               : nullptr;
   p.N = N;
   p.K = K;
   p.T = (N + kTileRows - 1) / kTileRows;
@@ -408,8 +471,25 @@ static int run_gemv(int bits, int pro, const void* wpacked, size_t wpacked_bytes
   p.red_offset = red_offset(M, K, fused, cfg.consumer);
   p.ring_offset = ring_offset(M, K, fused, cfg.consumer);
   p.launch_id = g_launch_counter.fetch_add(1, std::memory_order_relaxed) & 0x7fffffff;
+  plan_next_prefetch(p, next, M, fused);
+  p.wait_ns = wait_bound_ns();
+  const int fk = g_fault_kind.load(std::memory_order_relaxed);
+  p.fault = (fk == 1 || fk == 2) ? fk : 0;
+  p.fault_cta = (uint32_t)g_fault_cta.load(std::memory_order_relaxed);
   const cudaError_t e = launch_gemv_any(bits, pro, cfg.consumer, M, p, cfg, stream);
   return cuda_result(e);
+}
+
+int woq_prefetch_next(const void* next_wpacked, size_t next_wpacked_bytes, int bits, int N, int K, int budget_kb) {
+  if (!next_wpacked) {
+    t_next = NextHint{nullptr, 0, 0, 0, 0};
+    return WOQ_OK;
+  }
+  if ((bits != 4 && bits != 6) || N < 0 || K < 0 || K % kGroup || budget_kb < 0 || budget_kb > 65536) return WOQ_ERR_SHAPE;
+  if (!aligned(next_wpacked, 16)) return WOQ_ERR_ALIGN;
+  if (next_wpacked_bytes < packed_bytes(bits, N, K)) return WOQ_ERR_LAYOUT;
+  t_next = NextHint{next_wpacked, bits, N, K, budget_kb};
+  return WOQ_OK;
 }
 
 int woq_w4a8_gemv(const void* wpacked, size_t wpacked_bytes, const int8_t* q, const float* ascale, int M, int N,
@@ -482,6 +562,7 @@ int woq_debug_group_dots(int bits, const void* wpacked, size_t wpacked_bytes, co
 // file-scope device array below, part of this library's image on every GPU that
 // loads it and kept until the process exits.
 static constexpr size_t kNoAllocScratchBytes = 2u << 20;  // 2 MiB
+static constexpr size_t kNoAllocPartsOffset = 256;         // split-tile words: the workspace layout's parts_offset
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
@@ -520,21 +601,37 @@ int woq_w4a8_linear_bf16_noalloc(const void* wpacked, size_t wpacked_bytes, cons
   if (!y || (K > 0 && (!wpacked || !x_bf16))) return WOQ_ERR_NULL;
   if (!aligned(y, 4) || (K > 0 && (!aligned(wpacked, 16) || !aligned(x_bf16, 16)))) return WOQ_ERR_ALIGN;
   if (K > 0 && wpacked_bytes < packed_bytes(4, N, K)) return WOQ_ERR_LAYOUT;
-  // the scratch this launch will use must fit in the static array
+  // the scratch this launch will use must fit in the static array (the same rule run_gemv applies)
   size_t need = 256;
   if (K > 0) {
     const LaunchConfig cfg = choose_config(4, M, N, K, true);
     if (cfg.ctas <= 0) return WOQ_ERR_SHAPE;
-    need = workspace_layout(M, N, K, cfg.ctas).h_offset;  // the bf16 entry uses no scratch rows
+    if (cfg.ctas > max_ctas_for_workspace()) return WOQ_ERR_WORKSPACE;
+    need = workspace_need(kern::kProBf16, workspace_layout(M, N, K, cfg.ctas));
   }
   if (need > kNoAllocScratchBytes) return WOQ_ERR_WORKSPACE;
   void* ws = nullptr;
   const int st = noalloc_scratch(&ws);
   if (st != WOQ_OK) return st;
-  // the array keeps the previous call's contents: start from zero (no allocation involved)
-  if (const cudaError_t e_ = cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream); e_ != cudaSuccess) return cuda_result(e_);
+  // The array keeps the previous call's contents: the split-tile words start from zero (no
+  // allocation involved).  The status word (bytes 0 .. 3) is left alone: it keeps device-side
+  // errors until woq_noalloc_read_status clears it.
+  if (need > kNoAllocPartsOffset) {
+    if (const cudaError_t e_ = cudaMemsetAsync(static_cast<uint8_t*>(ws) + kNoAllocPartsOffset, 0,
+                                               need - kNoAllocPartsOffset, (cudaStream_t)stream);
+        e_ != cudaSuccess)
+      return cuda_result(e_);
+  }
   return run_gemv(4, kern::kProBf16, wpacked, wpacked_bytes, x_bf16, nullptr, nullptr, nullptr, 0.0f, M, N, K, y, ws,
                   kNoAllocScratchBytes, (cudaStream_t)stream);
+}
+
+int woq_noalloc_read_status(int clear, uint32_t* status_out, woq_stream_t stream) {
+  if (!status_out) return WOQ_ERR_NULL;
+  void* ws = nullptr;
+  const int st = noalloc_scratch(&ws);
+  if (st != WOQ_OK) return st;
+  return woq_read_status(ws, kNoAllocScratchBytes, clear, status_out, stream);
 }
 
 }  // extern "C"

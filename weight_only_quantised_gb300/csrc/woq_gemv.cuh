@@ -80,6 +80,18 @@ struct GemvParams {
   int red_offset;
   int ring_offset;
   int launch_id;            // trace builds only: which trace slot this launch writes
+  // The linear that runs after this one (a hint, may be null): once its own weight stream
+  // is issued, CTA c brings into L2 the first nx_blocks blocks, in processing order, of the
+  // range that CTA c of that launch will stream (its grid nx_C, nx_NB blocks of nx_bb bytes).
+  const uint8_t* nx_w;
+  uint32_t nx_NB, nx_C, nx_bb, nx_blocks;
+  FastDiv nx_div_c, nx_div_g;
+  // Bound of the waits on other CTAs of this grid (partner words, SwiGLU arrivals), and a
+  // fault to inject for tests of those bounds: 1 = CTA fault_cta never publishes its
+  // split-tile partials, 2 = it never counts itself in at the SwiGLU row maxima (0 = none).
+  uint64_t wait_ns;
+  int fault;
+  uint32_t fault_cta;
 };
 
 #ifdef WOQ_TRACE
@@ -429,6 +441,39 @@ struct StageCursor {
     }
   }
 };
+
+// L2 prefetch of the next linear's weights ("What is the bottleneck?": a decode step is a
+// run of weight reads, one linear after another).  A launch leaves the memory idle from
+// the moment its last weights have landed until the next launch's CTAs have started and
+// issued their own stream; the next launch's first stages are fetched in that gap instead.
+// CTA c takes the range CTA c of the next launch will stream (the same even partition) and
+// prefetches its first nx_blocks blocks in that launch's processing order (the partial
+// tile at the start of the range, the one at its end, then the whole tiles), in pieces of
+// at most 32 KiB.  Issued by the producer lane after the last copy of this launch's own
+// stream, so these bytes queue behind this launch's.
+static __device__ __noinline__ void prefetch_next_linear(const GemvParams& p, uint32_t cta) {
+  const uint32_t bb = range_begin(cta, p.nx_NB, p.nx_div_c);
+  const uint32_t be = range_begin(cta + 1, p.nx_NB, p.nx_div_c);
+  if (be <= bb) return;
+  const ItemOrder o(bb, be, p.nx_div_g);
+  const uint8_t* blocks = p.nx_w + kHeaderBytes;
+  uint32_t left = p.nx_blocks;
+  const uint32_t per_piece = (32u * 1024u) / p.nx_bb > 0 ? (32u * 1024u) / p.nx_bb : 1u;
+  for (int i = 0; i < o.n_items && left > 0; ++i) {
+    uint32_t t;
+    int ga, gb;
+    o.get(i, t, ga, gb);
+    uint32_t b = t * (uint32_t)o.G + (uint32_t)ga;
+    uint32_t n = (uint32_t)(gb - ga) < left ? (uint32_t)(gb - ga) : left;
+    left -= n;
+    while (n > 0) {
+      const uint32_t k = n < per_piece ? n : per_piece;
+      dev::bulk_prefetch_l2(blocks + (size_t)b * p.nx_bb, k * p.nx_bb);
+      b += k;
+      n -= k;
+    }
+  }
+}
 
 // Activation prologue of the fused entry, run by the consumer warps on the bf16 x
 // that one bulk copy placed at act[0, 2 M K) (or, with X_GLOBAL, on x in global
@@ -868,7 +913,8 @@ __device__ __forceinline__ uint4 swiglu8(const float* __restrict__ g, const floa
 // the end of the launch (swiglu_sync_reset).
 template <int M>
 __device__ __forceinline__ void swiglu_grid_max(uint32_t* sync, uint32_t C, const uint32_t (&acc)[M], int tid,
-                                                int lane, float* s_scratch, volatile int* s_ok, int launch_id) {
+                                                int lane, float* s_scratch, volatile int* s_ok, uint64_t wait_ns,
+                                                bool skip_arrival, int launch_id) {
   uint32_t* s_max = reinterpret_cast<uint32_t*>(s_scratch);  // [M] this CTA's largest |h| bits
 #pragma unroll
   for (int m = 0; m < M; ++m) {
@@ -880,11 +926,11 @@ __device__ __forceinline__ void swiglu_grid_max(uint32_t* sync, uint32_t C, cons
     WOQ_TRACE_EV2(61);
     for (int m = 0; m < M; ++m)
       if (s_max[m]) dev::red_max_relaxed_u32(sync + 8 + m, s_max[m]);
-    dev::red_add_release_u32(sync, 1u);  // ordered after the maxima
+    if (!skip_arrival) dev::red_add_release_u32(sync, 1u);  // ordered after the maxima
     bool ok = true;
     const uint64_t t0 = dev::global_timer_ns();
     while (dev::ld_acquire_u32(sync) < C) {
-      if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) {
+      if (dev::global_timer_ns() - t0 > wait_ns) {
         ok = false;
         break;
       }
@@ -904,7 +950,7 @@ __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs
                                                      uint32_t* sync, uint16_t* hbuf, uint32_t cta, uint32_t C,
                                                      int klo1, int khi1, int klo2, int khi2, int tid, int lane,
                                                      int warp, float* s_scratch, float* s_as, volatile int* s_ok,
-                                                     int launch_id) {
+                                                     uint64_t wait_ns, bool skip_arrival, int launch_id) {
   constexpr int kStride = kConsumers * 8;
   constexpr int kHV = M <= 4 ? 4 / M : 1;  // vectors per row and range kept in registers
   uint32_t* s_max = reinterpret_cast<uint32_t*>(s_scratch);
@@ -926,7 +972,7 @@ __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs
       acc[m] = absmax8(acc[m], h);
     }
   }
-  swiglu_grid_max<M>(sync, C, acc, tid, lane, s_scratch, s_ok, launch_id);  // also publishes the slices
+  swiglu_grid_max<M>(sync, C, acc, tid, lane, s_scratch, s_ok, wait_ns, skip_arrival, launch_id);  // also publishes the slices
   if (!*s_ok) return 0;
   // h of the k ranges this CTA's blocks read, written by the CTAs that own those slices
   // (read through L2: this SM's L1 may hold an older launch's lines)
@@ -985,10 +1031,10 @@ __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs
 // End of a launch with the split SwiGLU prologue: CTA 0 waits (bounded) until every CTA
 // has read the row maxima, then zeroes the words for the next launch.  false on timeout.
 template <int M>
-__device__ __forceinline__ bool swiglu_sync_reset(uint32_t* sync, uint32_t C) {
+__device__ __forceinline__ bool swiglu_sync_reset(uint32_t* sync, uint32_t C, uint64_t wait_ns) {
   const uint64_t t0 = dev::global_timer_ns();
   while (dev::ld_acquire_u32(sync + 2) < C)
-    if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) return false;
+    if (dev::global_timer_ns() - t0 > wait_ns) return false;
   sync[0] = 0u;
   sync[2] = 0u;
 #pragma unroll
@@ -1083,6 +1129,9 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
           ok = false;
           break;
         }
+        // consumers that gave up release slots without waiting for them to land: issue
+        // nothing more into the ring (the flag is written before any such release)
+        if (s_flags[1]) break;
         const uint32_t bytes = (uint32_t)(ld.nb() * BB);
         dev::mbar_arrive_expect_tx(full + slot, bytes);
         dev::bulk_copy_g2s(ring + (size_t)slot * kStageBytes, blocks + (size_t)ld.block() * BB, bytes, full + slot, pol);
@@ -1097,6 +1146,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
         }
       }
       WOQ_TRACE_EV(9);
+      if (ok && p.nx_w != nullptr && cta < p.nx_C) prefetch_next_linear(p, cta);
       if (!ok) atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
       // no bulk copy may still be landing in this CTA's shared memory when it exits
       dev::mbar_wait_bounded(actbar, 0);
@@ -1238,7 +1288,8 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
   if constexpr (PRO == kProSwiglu) {
     const int route = swiglu_split_prologue<M>(act, p.K, p.act_stride, static_cast<const float*>(p.x), p.sync,
                                                p.hbuf, cta, C, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch,
-                                               s_as, s_flags + 3, p.launch_id);
+                                               s_as, s_flags + 3, p.wait_ns, p.fault == 2 && cta == p.fault_cta,
+                                               p.launch_id);
     if (route == 2)
       quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
                            p.launch_id, s_scratch + 8);
@@ -1377,7 +1428,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
         const int first_part = item == 0 ? fp0 : fp1;
         const bool comb = item == 0 ? comb0 : comb1;
         if (!comb) {
-          if (write_ok) {
+          if (write_ok && !(p.fault == 1 && cta == p.fault_cta)) {
             const int part = (t == order.first_tile) ? 0 : 1;
             unsigned long long* mine = p.parts + ((size_t)(cta * 2 + part) * M) * kTileRows;
 #pragma unroll
@@ -1423,7 +1474,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
                 if (!(v >> 32)) {
                   const uint64_t t0 = dev::global_timer_ns();
                   while (!(v >> 32)) {
-                    if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) break;
+                    if (dev::global_timer_ns() - t0 > p.wait_ns) break;
                     __nanosleep(64);
                     v = dev::ld_relaxed_u64(src[b] + m * kTileRows);
                   }
@@ -1447,7 +1498,7 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
     }
   }
   if constexpr (PRO == kProSwiglu) {
-    if (cta == 0 && tid == 0 && s_flags[3] && !swiglu_sync_reset<M>(p.sync, C))
+    if (cta == 0 && tid == 0 && s_flags[3] && !swiglu_sync_reset<M>(p.sync, C, p.wait_ns))
       atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
   }
   if (tid == 0) WOQ_TRACE_EV(8);

@@ -56,7 +56,9 @@ cudaError_t launch_group_dots(int bits, const void* wpacked, const int8_t* q, in
                               cudaStream_t stream);
 cudaError_t launch_pack_device(int bits, const uint8_t* q, const uint16_t* scales, int N, int K, void* dst,
                                cudaStream_t stream);
-// in-place relayout; *too_large = 1 (and nothing launched) if the staging does not fit
-cudaError_t launch_relayout(int bits, void* buf, int N, int K, int* too_large, cudaStream_t stream);
+// in-place relayout; *too_large = 1 (and nothing launched) if the staging does not fit.  wait_ns bounds
+// the waits on other CTAs; fault_cta >= 0 injects a CTA that never arrives (tests of that bound).
+cudaError_t launch_relayout(int bits, void* buf, int N, int K, int* too_large, cudaStream_t stream,
+                            unsigned long long wait_ns, int fault_cta);
 
 }  // namespace woq

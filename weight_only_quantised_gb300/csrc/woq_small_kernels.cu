@@ -329,11 +329,13 @@ struct RelayoutPlan {
   int tiles_per_batch;  // whole tiles per batch, batches from the top down
   int q_slots;          // blocks a CTA stages per batch
   int scale_slots;      // blocks whose scales a CTA stages for the whole run
+  unsigned long long wait_ns;  // bound of every wait on the other CTAs
+  int fault_cta;               // tests of that bound: this CTA leaves before the first barrier (-1: none)
 };
 
 
 // Grid barrier on words[0] (arrivals) and words[1] (generation); bounded.
-__device__ bool rl_grid_barrier(uint32_t* words, int* s_ok) {
+__device__ bool rl_grid_barrier(uint32_t* words, int* s_ok, unsigned long long wait_ns) {
   __syncthreads();
   if (threadIdx.x == 0) {
     bool ok = true;
@@ -346,7 +348,7 @@ __device__ bool rl_grid_barrier(uint32_t* words, int* s_ok) {
     } else {
       const uint64_t t0 = dev::global_timer_ns();
       while (dev::ld_acquire_u32(words + 1) == gen) {
-        if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) {
+        if (dev::global_timer_ns() - t0 > wait_ns) {
           ok = false;
           break;
         }
@@ -404,7 +406,8 @@ __global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, Rela
     }
     slot += i_hi - i_lo;
   }
-  if (!rl_grid_barrier(words, &s_ok)) return;
+  if (cta == pl.fault_cta) return;  // injected fault: never arrives, the others' waits run out
+  if (!rl_grid_barrier(words, &s_ok, pl.wait_ns)) return;
 
   slot = 0;
   // this thread's chunk of every block: four consecutive lanes take the four 32-k quarters of
@@ -439,7 +442,7 @@ __global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, Rela
           *reinterpret_cast<uint2*>(sb + hi_chunk_offset(c4, j, l)) = make_uint2(hi[0], hi[1]);
       }
     }
-    if (!rl_grid_barrier(words, &s_ok)) return;  // every canonical byte of the batch has been read
+    if (!rl_grid_barrier(words, &s_ok, pl.wait_ns)) return;  // every canonical byte of the batch has been read
     int k = 0;
     for (int i = i_lo; i < i_hi; ++i, ++k, ++slot) {
       uint8_t* out = buf + kHeaderBytes + (size_t)(tlo * pl.G + i) * BB;
@@ -459,7 +462,7 @@ __global__ void __launch_bounds__(kRlThreads) relayout_kernel(uint8_t* buf, Rela
     bool ok = true;
     const uint64_t t0 = dev::global_timer_ns();
     while (dev::ld_acquire_u32(words + 3) != (uint32_t)C) {
-      if (dev::global_timer_ns() - t0 > dev::kWaitLimitNs) {
+      if (dev::global_timer_ns() - t0 > pl.wait_ns) {
         ok = false;
         break;
       }
@@ -587,7 +590,7 @@ namespace woq {
 // Relayout plan: batches of whole tiles whose staged blocks fit next to all of the CTA's
 // staged scales; 0 tiles per batch if even one tile does not fit.
 static kern::RelayoutPlan relayout_plan(int bits, int N, int K, int ctas, int smem) {
-  kern::RelayoutPlan pl = {N, K, (N + kTileRows - 1) / kTileRows, K / kGroup, 0, 0, 0};
+  kern::RelayoutPlan pl = {N, K, (N + kTileRows - 1) / kTileRows, K / kGroup, 0, 0, 0, dev::kWaitLimitNs, -1};
   const int QB = block_bytes(bits) - kScaleBytes;
   for (int tb = pl.T; tb >= 1; --tb) {
     int scale_slots = 0, q_slots = 0;
@@ -607,7 +610,8 @@ static kern::RelayoutPlan relayout_plan(int bits, int N, int K, int ctas, int sm
   return pl;
 }
 
-cudaError_t launch_relayout(int bits, void* buf, int N, int K, int* too_large, cudaStream_t stream) {
+cudaError_t launch_relayout(int bits, void* buf, int N, int K, int* too_large, cudaStream_t stream,
+                            unsigned long long wait_ns, int fault_cta) {
   *too_large = 0;
   int dev = 0, sms = 0, smem = 0, coop = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -647,6 +651,8 @@ cudaError_t launch_relayout(int bits, void* buf, int N, int K, int* too_large, c
   if (e != cudaSuccess) return e;
   uint8_t* b = static_cast<uint8_t*>(buf);
   kern::RelayoutPlan plan = pl;
+  plan.wait_ns = wait_ns;
+  plan.fault_cta = fault_cta;
   void* args[] = {(void*)&b, (void*)&plan, (void*)&h};
   return cudaLaunchCooperativeKernel(func, dim3((unsigned)sms), dim3(kern::kRlThreads), args, dyn, stream);
 }
