@@ -60,6 +60,12 @@ def parse_args():
                     help="time the in-place relayout of 27B-class matrices instead of the step")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
                     help="with --linear: int4 consumer (0 launch table, 1 dp4a, 2 tensor-core MMA)")
+    ap.add_argument("--shape", default="27b", choices=["27b", "9b"], help="with --linear: 27B- or 9B-class shapes")
+    ap.add_argument("--suite", action="store_true",
+                    help="time the 1024 x 1024 linear, the 9B W4A8 linears (M = 1, 3) and the 9B W6A8 linears "
+                         "(M = 1 .. 4) instead of the step")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the per-linear config suite on the headline line")
     return ap.parse_args()
 
 
@@ -213,6 +219,7 @@ class Step:
             del w, s
         torch.cuda.synchronize()
         self.graphs = {}
+        self.prefetch_next_kb = 0  # next-linear L2 prefetch per CTA (KiB, 0 = library default, -1 = off)
 
     def buffers(self, M, seed=2):
         torch, synthetic, woq = self.torch, self.synthetic, self.woq
@@ -226,7 +233,11 @@ class Step:
 
     def launch_all(self, xs, ys, ws):
         woq = self.woq
-        for (name, K, N), p in zip(self.linears, self.packed):
+        n = len(self.linears)
+        for i, ((name, K, N), p) in enumerate(zip(self.linears, self.packed)):
+            if self.prefetch_next_kb >= 0 and i + 1 < n:
+                _, K2, N2 = self.linears[i + 1]
+                woq.woq_prefetch_next(self.packed[i + 1], 4, N2, K2, self.prefetch_next_kb)
             woq.woq_w4a8_linear_bf16(p, xs[K], N, K, ys[N], ws)
 
     def time_prologue_chain(self, M, steps, warmup, fused):
@@ -350,18 +361,42 @@ class Step:
         return dt, h2d, d2h
 
 
-def cpu_baseline_oracle(sample, M, seed=2):
-    """The oracle (single thread, as it stands) on 1/div of every linear's rows, M activation rows."""
+def host_cores():
+    """CPU cores this process may run on (sched_getaffinity), or the CPU count."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_oracle(sample, M, threads=1, seed=2):
+    """The oracle, as it stands, on 1/div of every linear's rows, M activation rows.  threads > 1
+    splits each linear's rows into that many slices run by Python threads (the oracle is C
+    called through ctypes, which releases the GIL, so the slices run in parallel)."""
+    import concurrent.futures as cf
+
     import oracle
     import synthetic
     xs = {}
-    total_bytes = 0
-    t0 = time.perf_counter()
-    for K, rows, wn, sn in sample:
+    for K, *_ in sample:
         if K not in xs:
             xs[K] = synthetic.to_numpy_u16(synthetic.activations(M, K, synthetic.sub_seed(seed, "x", M, K)))
-        oracle.linear_bf16(4, wn, sn, rows, K, xs[K])
+    jobs = []
+    total_bytes = 0
+    for K, rows, wn, sn in sample:
         total_bytes += rows * K // 2 + 2 * rows * (K // 128) + 2 * M * K
+        n = max(1, min(threads, rows))
+        for t in range(n):
+            r0, r1 = rows * t // n, rows * (t + 1) // n
+            if r1 > r0:
+                jobs.append((K, r1 - r0, wn[r0:r1], sn[r0:r1]))
+    t0 = time.perf_counter()
+    if threads == 1:
+        for K, r, wn, sn in jobs:
+            oracle.linear_bf16(4, wn, sn, r, K, xs[K])
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda j: oracle.linear_bf16(4, j[2], j[3], j[1], j[0], xs[j[0]]), jobs))
     dt = time.perf_counter() - t0
     return total_bytes / dt / 1e9, dt, total_bytes
 
@@ -421,12 +456,20 @@ def run_ours(args):
         e2e = {"value": round(world * bytes_step / dt / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 4)}
 
+    configs = None
+    if args.configs and rank == 0:
+        configs = config_suite(steps=30, warmup=3)
+
     cpu = None
     if do_cpu:
-        v, dt, nbytes = cpu_baseline_oracle(step.cpu_sample, M)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"first 1/{args.cpu_sample_div} of the rows of all 257 linears of the step, M={M} "
-                         f"({nbytes / 1e9:.2f} GB of weights+scales, {dt:.1f} s, single thread)"}
+        cores = host_cores()
+        v1, dt1, nbytes = cpu_baseline_oracle(step.cpu_sample, M, threads=1)
+        vn, dtn, _ = cpu_baseline_oracle(step.cpu_sample, M, threads=cores)
+        what = (f"first 1/{args.cpu_sample_div} of the rows of all 257 linears of the step, M={M} "
+                f"({nbytes / 1e9:.2f} GB of weights+scales)")
+        cpu = {"value": round(vn, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{what}; {cores} threads (one per core from sched_getaffinity), {dtn:.1f} s",
+               "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1, "seconds": round(dt1, 1)}}
 
     peak, peak_kind = measured_peak()
     achieved = bytes_step / (ms_step * 1e-3) / 1e9
@@ -456,8 +499,11 @@ def run_ours(args):
                      "per": "step (257 launches)"},
         "extra_m": extra,
         "prologue_fusion": prologue,
+        "configs": configs,
         "e2e": e2e,
         "gpu_launches": len(step.linears) * args.steps,
+        "prefetch_next": {"kb_per_cta": "library default", "what": "each launch prefetches the next linear's "
+                                                                  "first weights into L2 (woq_prefetch_next)"},
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -471,7 +517,8 @@ def run_ours(args):
 
 def run_reference(args):
     """The CPU oracle on the host cores: each step is a bounded row sample of one of the
-    step's linears (cycling through all 257), sized so the whole run takes about a minute."""
+    step's linears (cycling through all 257), sized so the whole run takes about a minute; the
+    sample's rows are split over one thread per core (the C oracle runs without the GIL)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -488,19 +535,25 @@ def run_reference(args):
     oracle.linear_bf16(4, w.numpy(), synthetic.to_numpy_u16(s), N0, K0, x)
     rate = N0 * K0 / max(time.perf_counter() - t0, 1e-6)  # weights per second
     budget = 60.0 / max(1, args.steps + args.warmup)
+    cores = host_cores()
+    import concurrent.futures as cf
+    pool = cf.ThreadPoolExecutor(max_workers=cores)
     cache = {}
     total_b, total_t = 0, 0.0
     for i in range(args.warmup + args.steps):
         name, K, N = linears[i % len(linears)]
-        rows = int(min(N, max(1, budget * rate / K)))
+        rows = int(min(N, max(cores, budget * rate * cores / K)))
         key = (name, rows)
         if key not in cache:
             wt, st = synthetic.weights(4, rows, K, synthetic.sub_seed(2, name, rows))
             xk = synthetic.to_numpy_u16(synthetic.activations(M, K, synthetic.sub_seed(2, "x", M, K)))
             cache = {key: (wt.numpy(), synthetic.to_numpy_u16(st), xk)}
         wn, sn, xk = cache[key]
+        cuts = [rows * t // cores for t in range(cores + 1)]
         t0 = time.perf_counter()
-        oracle.linear_bf16(4, wn, sn, rows, K, xk)
+        list(pool.map(lambda t: oracle.linear_bf16(4, wn[cuts[t]:cuts[t + 1]], sn[cuts[t]:cuts[t + 1]],
+                                                   cuts[t + 1] - cuts[t], K, xk),
+                      [t for t in range(cores) if cuts[t + 1] > cuts[t]]))
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             total_t += dt
@@ -523,38 +576,42 @@ def run_reference(args):
         "data": "synthetic (seeded; random weights of the 27B-class shapes)",
         "config": {"workload": WORKLOAD, "m": M, "linears": len(linears),
                    "sample": "each step: a row sample of one linear of the step, cycling through all 257"},
-        "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(value, 4), "unit": "GB/s",
-                         "sample": f"{args.steps} steps of row samples (~{budget:.2f} s each), single thread"},
+        "cpu_baseline": {"kind": "oracle", "cores": cores, "value": round(value, 4), "unit": "GB/s",
+                         "sample": f"{args.steps} steps of row samples (~{budget:.2f} s each), {cores} threads "
+                                   f"(one per core from sched_getaffinity)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    pool.shutdown()
     print(json.dumps(line), flush=True)
 
 
-def run_linear(args):
-    """One linear of the 27B-class step, launched back to back over enough distinct packed
-    copies that their total exceeds 1 GB (every launch streams its weights from HBM)."""
+L2_BYTES = 129 * 2 ** 20  # GB300 L2
+
+
+def time_linear_chain(bits, M, K, N, entry="bf16", seed=2, steps=50, warmup=3, path=0, name="linear",
+                      rotation_bytes=int(1.2e9)):
+    """One linear launched back to back over distinct packed copies of its weights whose total is
+    at least rotation_bytes (>= 4 x L2 by default: every launch streams its weights from HBM, the
+    cold-L2 rule), captured in one CUDA graph and replayed steps times.  entry: "bf16" (fused
+    quant + GEMV), "int8" (act_quant once, then the GEMV), "rmsnorm" or "swiglu" (the prologue
+    fusions).  Returns a dict with the time per launch and the algorithmic bandwidth."""
     import torch
 
     import synthetic
     import weight_only_quantised_gb300 as woq
-    shapes = dict(synthetic.LINEARS_27B)
-    shapes["lm_head"] = synthetic.LM_HEAD_27B
-    K, N = shapes[args.linear]
-    M = args.m
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    woq.woq_tune_path(args.path)
-    bits = args.bits
+    assert rotation_bytes >= 4 * L2_BYTES
+    dev = torch.device("cuda", torch.cuda.current_device())
+    woq.woq_tune_path(path)
     pb = woq.woq_packed_bytes(bits, N, K)
-    copies = max(4, int(1.2e9 // pb))
-    w, s = synthetic.weights(bits, N, K, synthetic.sub_seed(2, args.linear), device=dev)
+    copies = max(4, -(-rotation_bytes // pb))
+    w, s = synthetic.weights(bits, N, K, synthetic.sub_seed(seed, name, bits), device=dev)
     bufs = []
     for _ in range(copies):
         p = torch.empty(pb, dtype=torch.uint8, device=dev)
         woq.woq_pack_device(bits, w, s.view(torch.int16), N, K, p)
         bufs.append(p)
     del w, s
-    x = synthetic.activations(M, K, synthetic.sub_seed(2, "x", M, K), device=dev)
+    x = synthetic.activations(M, K, synthetic.sub_seed(seed, "x", M, K), device=dev)
     q = torch.empty((M, K), dtype=torch.int8, device=dev)
     a = torch.empty((M,), dtype=torch.float32, device=dev)
     woq.woq_act_quant_int8(x, q, a)
@@ -562,16 +619,15 @@ def run_linear(args):
     ws = torch.zeros(woq.woq_workspace_bytes(bits, M, N, K), dtype=torch.uint8, device=dev)
     gamma = synthetic.rmsnorm_weight(K, 9, device=dev)
     gu = synthetic.gate_up_output(M, K, 9, device=dev)
-
     w4 = bits == 4
 
     def launch(p):
-        if args.int8:
+        if entry == "int8":
             (woq.woq_w4a8_gemv if w4 else woq.woq_w6a8_gemv)(p, q, a, N, K, y, ws)
-        elif args.prologue == "rmsnorm":
+        elif entry == "rmsnorm":
             (woq.woq_w4a8_linear_rmsnorm_bf16 if w4 else woq.woq_w6a8_linear_rmsnorm_bf16)(p, x, gamma, 1e-6, N, K,
                                                                                          y, ws)
-        elif args.prologue == "swiglu":
+        elif entry == "swiglu":
             (woq.woq_w4a8_linear_swiglu_f32 if w4 else woq.woq_w6a8_linear_swiglu_f32)(p, gu, N, K, y, ws)
         else:
             (woq.woq_w4a8_linear_bf16 if w4 else woq.woq_w6a8_linear_bf16)(p, x, N, K, y, ws)
@@ -583,25 +639,76 @@ def run_linear(args):
     with torch.cuda.graph(g, stream=st):
         for p in bufs:
             launch(p)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
+    for _ in range(steps):
         g.replay()
     e1.record()
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / (args.steps * copies)
-    act_bytes = {"none": 2 * M * K, "rmsnorm": 2 * M * K + 2 * K, "swiglu": 8 * M * K}[args.prologue]
-    nbytes = N * K * bits // 8 + 2 * N * (K // 128) + (M * K if args.int8 else act_bytes)
+    assert woq.woq_read_status(ws) == 0
+    woq.woq_tune_path(0)
+    us = e0.elapsed_time(e1) * 1e3 / (steps * copies)
+    act_bytes = {"bf16": 2 * M * K, "rmsnorm": 2 * M * K + 2 * K, "swiglu": 8 * M * K, "int8": M * K + 4 * M}[entry]
+    nbytes = N * K * bits // 8 + 2 * N * (K // 128) + act_bytes
     peak, kind = measured_peak()
-    entry = "int8" if args.int8 else {"none": "bf16", "rmsnorm": "rmsnorm_bf16", "swiglu": "swiglu_f32"}[args.prologue]
-    print(json.dumps({"linear": args.linear, "K": K, "N": N, "m": M, "bits": bits, "entry": entry,
-                      "consumer": {0: "table", 1: "dp4a", 2: "mma"}[args.path],
-                      "us_per_launch": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
-                      "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "peak_kind": kind,
-                      "launches_per_graph": copies}), flush=True)
+    del bufs
+    torch.cuda.empty_cache()
+    return {"linear": name, "K": K, "N": N, "m": M, "bits": bits, "entry": entry,
+            "us_per_launch": round(us, 3), "gbs": round(nbytes / us / 1e3, 1),
+            "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "peak_kind": kind, "bytes_per_launch": nbytes,
+            "rotation": {"copies": copies, "bytes": copies * pb}}
+
+
+def config_suite(steps=30, warmup=3):
+    """The single 1024 x 1024 linear, the 9B-class layer's linears at M = 1 and 3 (W4A8), and the
+    9B-class linears in W6A8 at M = 1 .. 4 through the fused bf16 entry; each timed as a chain over
+    a cold-L2 rotation of distinct weight copies (>= 4 x L2)."""
+    import synthetic
+    out = {"w4a8_1024x1024": [time_linear_chain(4, 1, 1024, 1024, seed=0, steps=steps, warmup=warmup,
+                                                name="single_1024")]}
+    rows = []
+    for M in (1, 3):
+        for name, (K, N) in synthetic.LINEARS_9B.items():
+            rows.append(time_linear_chain(4, M, K, N, seed=1, steps=steps, warmup=warmup, name=name))
+    out["9b_w4a8"] = rows
+    rows = []
+    for M in (1, 2, 3, 4):
+        for name, (K, N) in synthetic.LINEARS_9B.items():
+            rows.append(time_linear_chain(6, M, K, N, seed=4, steps=steps, warmup=warmup, name=name))
+    out["9b_w6a8_fused"] = rows
+    for key, rows in out.items():
+        for r in rows:
+            r.pop("peak_kind", None)
+    return out
+
+
+def run_linear(args):
+    """One 27B-class linear (or, with --shape 9b, a 9B-class one), launched back to back over
+    distinct packed copies whose total exceeds 1 GB (every launch streams its weights from HBM)."""
+    import torch
+
+    import synthetic
+    shapes = dict(synthetic.LINEARS_9B if args.shape == "9b" else synthetic.LINEARS_27B)
+    shapes["lm_head"] = synthetic.LM_HEAD_27B
+    K, N = shapes[args.linear]
+    torch.cuda.set_device(torch.device("cuda", 0))
+    entry = "int8" if args.int8 else {"none": "bf16", "rmsnorm": "rmsnorm", "swiglu": "swiglu"}[args.prologue]
+    r = time_linear_chain(args.bits, args.m, K, N, entry=entry, seed=2, steps=args.steps, warmup=args.warmup,
+                          path=args.path, name=args.linear)
+    r["consumer"] = {0: "table", 1: "dp4a", 2: "mma"}[args.path]
+    print(json.dumps(r), flush=True)
+
+
+def run_suite(args):
+    """The configs other than the 27B step (see config_suite), one JSON line."""
+    import torch
+    torch.cuda.set_device(torch.device("cuda", 0))
+    peak, kind = measured_peak()
+    print(json.dumps({"metric": "per-linear time and algorithmic HBM GB/s, cold L2", "peak": peak, "peak_kind": kind,
+                      "configs": config_suite(steps=max(10, min(args.steps, 100)), warmup=args.warmup)}), flush=True)
 
 
 def run_tree_planner(args):
@@ -696,6 +803,9 @@ def main():
         return
     if args.linear:
         run_linear(args)
+        return
+    if args.suite:
+        run_suite(args)
         return
     if args.impl == "reference":
         run_reference(args)
