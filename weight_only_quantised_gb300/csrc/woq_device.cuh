@@ -120,23 +120,10 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t h16) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
-// Activation quantisation: q = rne(x / s), where x / s is the IEEE round-to-nearest
-// quotient, for a row scale s = amax / 127 != 0 and rc = the correctly rounded
-// reciprocal of s.  t = fl(x * rc) is within |x/s| (3u + u^2) (u = 2^-24) of fl(x / s),
-// below 2.28e-5 since |x/s| <= 127 (1 + 2u).  Unless t lies within 3e-5 of a tie
-// (|t - rne(t)| > 0.5 - 3e-5), t and fl(x / s) round to the same integer; the caller
-// takes the IEEE division for the rare values that are that close (or when rc
-// overflowed).  |t| < 127.5, so no clamp to [-127, 127] is ever needed.
+// Activation quantisation helpers.  The kernels' division-free code of x is rne of a
+// corrected quotient (woq_quotient.h); kRoundMagic turns a value below 2^22 in magnitude into
+// its rne in the low bits of the sum's pattern.
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: t + magic rounds t to an integer (RNE)
-constexpr float kTieGuard = 0.5f - 3e-5f;
-
-// Low byte (two's complement) of rne(t) for |t| < 2^22, and whether t is near a tie.
-__device__ __forceinline__ uint32_t quant_byte_fast(float t, bool& near_tie) {
-  const float y = __fadd_rn(t, kRoundMagic);
-  const float r = __fsub_rn(y, kRoundMagic);
-  near_tie = !(fabsf(__fsub_rn(t, r)) <= kTieGuard);  // NaN (rc = inf) counts as near
-  return (uint32_t)__float_as_int(y) & 0xFFu;
-}
 
 // Low byte of rne(fl(x / s)) by the IEEE division (the slow, always-exact route).
 __device__ __forceinline__ uint32_t quant_byte_exact(float x, float s) {

@@ -517,25 +517,23 @@ __device__ __forceinline__ void scale_and_rcp(float amax, float& s, float& rc) {
   }
 }
 
-// Eight bf16 values -> eight q bytes by the fast route, the pairs in packed fp32x2
-// arithmetic: t = RN(x rc); y = RN(t + 1.5 2^23), whose low byte is rne(t) mod 256;
-// d = t - rne(t) (exact); g = RN(d d - kTieGuard^2).  `gand` keeps the AND of the g
-// words: its sign bit stays set only while every |d| is below kTieGuard (with a margin
-// far above the rounding of g), i.e. while no value of the vector needs the exact route.
-__device__ __forceinline__ uint2 quantise8_fast(uint4 xv, dev::f32x2 rc2, uint32_t& gand) {
-  constexpr float kGuardSq = dev::kTieGuard * dev::kTieGuard;
+// Eight bf16 values -> eight q bytes, q = rne(RN(x / s)) without a division, the pairs in
+// packed fp32x2 arithmetic (woq_quotient.h): t = RN(x rc), r = RN(x - t s) by a fused
+// multiply-add, u = RN(t + r rc) (the correction step of Markstein's division), and
+// y = RN(u + 1.5 2^23), whose low byte is rne(u) mod 256.  ns2 holds -s.  rne(u) equals the
+// code of the IEEE quotient for every bf16 x with |x| <= amax whenever amax >= 2^-116
+// (row_fast); other rows take quantise8_exact.
+__device__ __forceinline__ uint2 quantise8_fast(uint4 xv, dev::f32x2 rc2, dev::f32x2 ns2) {
   const dev::f32x2 magic = dev::f2_splat(dev::kRoundMagic);
-  const dev::f32x2 nguard = dev::f2_splat(-kGuardSq);
   const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
   uint32_t yb[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const dev::f32x2 x = dev::f2_pack(w4[i] << 16, w4[i] & 0xFFFF0000u);  // values 2i, 2i+1
     const dev::f32x2 t = dev::f2_mul(x, rc2);
-    const dev::f32x2 y = dev::f2_add(t, magic);
-    const dev::f32x2 d = dev::f2_sub(t, dev::f2_sub(y, magic));
-    const dev::f32x2 g = dev::f2_fma(d, d, nguard);
-    gand &= dev::f2_lo(g) & dev::f2_hi(g);
+    const dev::f32x2 r = dev::f2_fma(t, ns2, x);
+    const dev::f32x2 u = dev::f2_fma(r, rc2, t);
+    const dev::f32x2 y = dev::f2_add(u, magic);
     yb[2 * i] = dev::f2_lo(y);
     yb[2 * i + 1] = dev::f2_hi(y);
   }
@@ -543,8 +541,8 @@ __device__ __forceinline__ uint2 quantise8_fast(uint4 xv, dev::f32x2 rc2, uint32
                     __byte_perm(__byte_perm(yb[4], yb[5], 0x0040), __byte_perm(yb[6], yb[7], 0x0040), 0x5410));
 }
 
-// Eight q bytes by the IEEE division; kept out of line so the common path carries no
-// division code.
+// Eight q bytes by the IEEE division, for rows with amax below 2^-116 (none in practice);
+// kept out of line so the common path carries no division code.
 static __device__ __noinline__ uint2 quantise8_exact(uint4 xv, float sc) {
   const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
   uint32_t qb[8];
@@ -612,9 +610,16 @@ __device__ __forceinline__ void given_row_scales(const float* amax_in, int tid, 
   }
 }
 
-// Fast-route gate of a row: all ones when the fast route may decide (rc finite; an
-// all-zero row has rc = 0), else zero so that every vector of the row is redone.
-__device__ __forceinline__ uint32_t row_gate(float rc) { return rc <= 3.4028234e38f ? 0xFFFFFFFFu : 0u; }
+// Whether a row's codes come from quantise8_fast: its scale s = RN(amax / 127) is zero (an
+// all-zero row: rc = 0 gives u = 0, q = 0) or at least 2^-123, i.e. amax >= 2^-116.  Uniform
+// across the row, so a warp never diverges on it.
+__device__ __forceinline__ bool row_fast(float s) { return s == 0.0f || s >= 0x1p-123f; }
+
+// Eight q bytes of one vector of a row: the division-free route or, for rows too small for
+// it, the IEEE division.
+__device__ __forceinline__ uint2 quantise8(uint4 xv, dev::f32x2 rc2, dev::f32x2 ns2, float s, bool fast) {
+  return fast ? quantise8_fast(xv, rc2, ns2) : quantise8_exact(xv, s);
+}
 
 // X_GLOBAL: rows that fit registers are read straight from x in global memory (L2 only: the
 // previous grid wrote them) instead of from a bf16 copy in shared memory; longer rows are not
@@ -657,34 +662,23 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
       row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
     }
     if (tid == 0) WOQ_TRACE_EV2(5);
-    dev::f32x2 rc2[M];
-    uint32_t gate[M];
+    dev::f32x2 rc2[M], ns2[M];
+    bool fast[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       rc2[m] = dev::f2_splat(rc[m]);
-      gate[m] = row_gate(rc[m]);
+      ns2[m] = dev::f2_splat(-sc[m]);
+      fast[m] = row_fast(sc[m]);
     }
-    uint32_t redo = 0;  // bit m * kVPR + j
 #pragma unroll
     for (int j = 0; j < kVPR; ++j) {
       if (kStride * j >= K) break;  // uniform
       const int k = 8 * tid + kStride * j;
       if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {  // read by this CTA
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-          uint32_t g = gate[m];
-          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(xv[m][j], rc2[m], g);
-          redo |= (~g >> 31) << (m * kVPR + j);
-        }
+        for (int m = 0; m < M; ++m)
+          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(xv[m][j], rc2[m], ns2[m], sc[m], fast[m]);
       }
-    }
-    if (__any_sync(0xffffffffu, redo != 0)) {  // rare
-#pragma unroll
-      for (int m = 0; m < M; ++m)
-#pragma unroll
-        for (int j = 0; j < kVPR; ++j)
-          if (redo & (1u << (m * kVPR + j)))
-            *reinterpret_cast<uint2*>(act + m * qs + 8 * tid + kStride * j) = quantise8_exact(xv[m][j], sc[m]);
     }
     return;
   }
@@ -712,7 +706,8 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
 #pragma unroll
   for (int m = 0; m < M; ++m) {
     const dev::f32x2 rc2 = dev::f2_splat(rc[m]);
-    const uint32_t gate = row_gate(rc[m]);
+    const dev::f32x2 ns2 = dev::f2_splat(-sc[m]);
+    const bool fast = row_fast(sc[m]);
     for (int k0 = 0; k0 < K; k0 += 4 * kStride) {
       // CTA-uniform: skip rounds that hold no k this CTA reads
       if (!((k0 < khi1 && k0 + 4 * kStride > klo1) || (k0 < khi2 && k0 + 4 * kStride > klo2))) continue;
@@ -723,21 +718,11 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
         xv[v] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
       }
       dev::named_barrier_sync(kBarConsumers, kConsumers);
-      uint32_t redo = 0;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const int k = k0 + 8 * tid + kStride * v;
-        if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {
-          uint32_t g = gate;
-          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(xv[v], rc2, g);
-          redo |= (~g >> 31) << v;
-        }
-      }
-      if (__any_sync(0xffffffffu, redo != 0)) {  // rare
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          if (redo & (1u << v))
-            *reinterpret_cast<uint2*>(act + m * qs + k0 + 8 * tid + kStride * v) = quantise8_exact(xv[v], sc[m]);
+        if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2)))
+          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(xv[v], rc2, ns2, sc[m], fast);
       }
     }
   }
@@ -874,15 +859,13 @@ __device__ __forceinline__ void rmsnorm_quantise_regs(uint8_t* act, int K, int q
     scale_and_rcp(__uint_as_float(s_bits[8 + m]), sc, rc);
     if (tid == 0) s_as[m] = sc;
     const dev::f32x2 rc2 = dev::f2_splat(rc);
-    const uint32_t gate = row_gate(rc);
+    const dev::f32x2 ns2 = dev::f2_splat(-sc);
+    const bool fast = row_fast(sc);
 #pragma unroll
     for (int j = 0; j < kRmsRegVecs; ++j) {
       const int k = 8 * tid + kStride * j;
-      if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {
-        uint32_t g = gate;
-        *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(v[m][j], rc2, g);
-        if (!(g >> 31)) *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_exact(v[m][j], sc);  // rare
-      }
+      if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2)))
+        *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(v[m][j], rc2, ns2, sc, fast);
     }
   }
 }
@@ -988,15 +971,15 @@ __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs
           for (int m = 0; m < M; ++m) hv[r][j][m] = __ldcg(reinterpret_cast<const uint4*>(hbuf + (size_t)m * K + k));
         }
       }
-    float sc[M];
-    dev::f32x2 rc2[M];
-    uint32_t gate[M];
+    float sc[M], rc[M];
+    dev::f32x2 rc2[M], ns2[M];
+    bool fast[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      float rc;
-      scale_and_rcp(s_scratch[8 + m], sc[m], rc);
-      rc2[m] = dev::f2_splat(rc);
-      gate[m] = row_gate(rc);
+      scale_and_rcp(s_scratch[8 + m], sc[m], rc[m]);
+      rc2[m] = dev::f2_splat(rc[m]);
+      ns2[m] = dev::f2_splat(-sc[m]);
+      fast[m] = row_fast(sc[m]);
     }
     if (tid < M) s_as[tid] = sc[tid];
 #pragma unroll
@@ -1006,11 +989,8 @@ __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs
         const int k = (r == 0 ? klo1 : klo2) + 8 * tid + j * kStride;
         if (k < (r == 0 ? khi1 : khi2)) {
 #pragma unroll
-          for (int m = 0; m < M; ++m) {
-            uint32_t gm = gate[m];
-            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(hv[r][j][m], rc2[m], gm);
-            if (!(gm >> 31)) *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_exact(hv[r][j][m], sc[m]);
-          }
+          for (int m = 0; m < M; ++m)
+            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(hv[r][j][m], rc2[m], ns2[m], sc[m], fast[m]);
         }
       }
     return 1;
