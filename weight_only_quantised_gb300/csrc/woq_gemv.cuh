@@ -54,7 +54,6 @@
 #include "woq_fastdiv.h"
 #include "woq_layout.h"
 #include "woq_prologue.cuh"
-#include "woq_scale_table.h"
 
 namespace woq {
 
@@ -494,23 +493,14 @@ static __device__ __noinline__ void prefetch_next_linear(const GemvParams& p, ui
 // quotient near a tie through the exact route, which stores them again.
 constexpr int kRegVecs = 12;  // 8-value vectors per thread kept in registers
 
-// Row scale s = RN(amax / 127) and rc = RN(1 / s) for a bf16 amax held in an fp32.
-// For 2^-119 <= amax < inf, amax = A 2^e with A = 1 + f/128 and the significand
-// tables hold RN(A / 127) and RN(1 / RN(A / 127)); a power of two passes through
-// round-to-nearest unchanged while the result stays normal, so both are exact.
-// An all-zero row gets s = 0 and rc = 0 (the fast route then yields q = 0); tiny and
-// non-finite amax take the IEEE division and reciprocal.
+// Row scale s = RN(amax / 127) and rc = RN(1 / s) for a bf16 amax held in an fp32, by the
+// IEEE division and reciprocal.  An all-zero row gets s = 0 and rc = 0 (quantise8_fast then
+// yields q = 0).  (Two constant tables of significands, read after a warm-up load, gave the
+// same bits; the step was 0.6 % slower at one row, 1.7 % at four.)
 __device__ __forceinline__ void scale_and_rcp(float amax, float& s, float& rc) {
-  const uint32_t b = __float_as_uint(amax);
-  const uint32_t e = b >> 23;  // biased exponent (amax >= 0)
-  if (e >= 8u && e < 255u) {
-    const uint32_t f = (b >> 16) & 0x7Fu;
-    const uint32_t sh = (e - 127u) << 23;  // two's complement exponent shift
-    s = __uint_as_float(kScaleSig[f] + sh);
-    rc = __uint_as_float(kRcpSig[f] - sh);
-  } else if (amax == 0.0f) {
-    s = 0.0f;   // all-zero row: q = 0
-    rc = 0.0f;  // so that the fast route gives t = 0, q = 0, far from any tie
+  if (amax == 0.0f) {
+    s = 0.0f;
+    rc = 0.0f;
   } else {
     s = __fdiv_rn(amax, 127.0f);
     rc = __frcp_rn(s);
@@ -1190,10 +1180,6 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
       }
     }
   }
-  // bring the row-scale tables into the constant cache: issued here, waited for only after the
-  // activations have landed, so a CTA that starts late does not pass the grid wait later
-  uint32_t warm = 0;
-  if constexpr (FUSED) warm = kScaleSig[(tid * 4) & 127] ^ kRcpSig[(tid * 4) & 127];
   // RMSNorm rows that fit registers: gamma (a weight) is loaded before the grid wait
   constexpr bool kRmsRegPath = PRO == kProRms && M <= 4;
   const bool rms_regs = kRmsRegPath && p.K <= kConsumers * 8 * kRmsRegVecs;
@@ -1244,7 +1230,6 @@ __global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
     s_flags[1] = 1;
     atomicOr(p.status, 0x2u /* WOQ_DEVERR_TIMEOUT */);
   }
-  asm volatile("" ::"r"(warm));
   if (tid == 0) {
     WOQ_TRACE_EV(4);
     // the packed header must describe this call's (bits, N, K)
