@@ -121,8 +121,8 @@ int smem_bytes_for(int bits, int M, int K, bool fused, int stages) {
 }
 
 // Shared memory a launch's ring and activations may take by default.  The kernel runs one CTA
-// per SM (nine warps at 112 registers: the 16,384-register file of a sub-partition holds four
-// such warps, so a second CTA never fits), and the next launch's CTA takes over an SM as soon
+// per SM (nine warps of 100 or more registers: the 16,384-register file of a sub-partition then
+// holds at most four, so a second CTA never fits), and the next launch's CTA takes over an SM as soon
 // as this launch's CTA there exits.  A ring deeper than this budget puts more of the next
 // launch's weights in the memory queues ahead of the running launch's activation and partial
 // reads: 27B step at M = 1 2.33 ms, 2.40-2.41 ms with four to seven stages everywhere.
@@ -141,7 +141,8 @@ LaunchConfig choose_config_for(int sms, int smem_max, int bits, int M, int N, in
   if (NB <= 0) return cfg;
   int cps = g_override_cps.load(std::memory_order_relaxed);
   // one CTA per SM is always resident (a CTA fits an SM alone or the launch fails); a second
-  // one never is at 112 registers, so a grid-wide step would wait for a wave that cannot start
+  // one never is (the kernels use 100 or more registers), so a grid-wide step would wait for a
+  // wave that cannot start
   if (cps <= 0 || resident_grid) cps = 1;
   const int ring_budget = kRingBudget < smem_max ? kRingBudget : smem_max;
   int stages = g_override_stages.load(std::memory_order_relaxed);

@@ -1017,10 +1017,14 @@ __device__ __forceinline__ bool swiglu_sync_reset(uint32_t* sync, uint32_t C, ui
 enum Consumer { kDp4a = 0, kMma = 1 };
 
 template <int BITS, int M, int PRO, int CONS>
-// 112 registers: one CTA per SM (a sub-partition's 16,384 registers hold four such warps, and
-// nine warps put three on one).  80, which lets two CTAs share an SM, spills and was slower
-// (27B step: M = 1 2.47 against 2.33 ms, M = 2 3.53 against 2.76 ms).
-__global__ void __maxnreg__(112) gemv_kernel(const GemvParams p) {
+// One CTA per SM: the nine warps put three on one sub-partition, whose 16,384 registers then
+// allow 168 per thread (3 x 32 x 168 = 16,128).  The cap was 112; at 168 the kernels use what
+// they need (114 at one row, 140 at four) and the 27B step got 0.2 % (M = 1) to 1.4 % (M = 3)
+// faster.  80, which let two CTAs share an SM, spilled and was slower (M = 1 2.47 against
+// 2.33 ms); 96 without spills let the next launch's CTA share the SM and was slower too (M = 1
+// 2.37 against 2.31 ms, M = 3 4.34 against 3.19): the next launch's ring fill then competes
+// with this launch's own stream.
+__global__ void __maxnreg__(168) gemv_kernel(const GemvParams p) {
   constexpr bool FUSED = PRO != kProInt8;  // activations quantised inside this launch
   static_assert(CONS == kDp4a || BITS == 4, "the tensor-core consumer reads int4 blocks");
   static_assert(CONS == kMma || M <= kMaxMDp4a, "dp4a kernels take up to four activation rows");
