@@ -287,7 +287,7 @@ WOQ_API int woq_noalloc_read_status(int clear, uint32_t* status_out, woq_stream_
  *   Tells the next GEMV / linear call made by this thread which linear will run
  *   after it: next_wpacked (device, the packed weights of (bits, N, K), at least
  *   woq_packed_bytes(bits, N, K) bytes).  That call, once its own weight stream has
- *   been issued, brings into L2 the first budget_kb KiB (0 = 48) of the weights
+ *   been issued, brings into L2 the first budget_kb KiB (0 = 64) of the weights
  *   each of the next launch's CTAs will stream first, planned as a launch of the
  *   same entry kind and M.  The next launch then finds them in L2; every weight
  *   byte is still read from HBM once.  A hint only: results are the same with or

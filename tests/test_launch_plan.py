@@ -6,9 +6,9 @@ derived by hand from the shared-memory layout:
     [activations: bf16 2 M K (fused entries) or int8 M x stride (stride K, K + 16 for the MMA
     consumer)][ring, from a 128-byte boundary: stages x 4 blocks of 8448 B (int4) / 12544 B (int6)]
 
-with the reduction buffer 4 x M x 128 x 4 bytes, up to four stages within 115,712 bytes (two
-rows: within the device limit), else the largest ring that fits; and against what ncu reported
-for the same launches on a GB300 (gate_up at M = 1: 112,640 B; LM head at M = 4: 109,568 B)."""
+with the reduction buffer 4 x M x 128 x 4 bytes, three stages (two rows, and five or more: four)
+within the device limit, else the largest ring that fits; and against what ncu reported for the
+same launches on a GB300 (gate_up at M = 1: 112,640 B)."""
 import pytest
 
 import weight_only_quantised_gb300 as woq
@@ -31,19 +31,19 @@ def table_defaults():
     (4, 1, 7168, 5120, 1, dict(ctas=152, stages=3, prefetch_stages=1, smem_bytes=112640, consumer=0)),
     # gate_up 5120 -> 34816: same layout; 10880 blocks >= 5000 at one row: two prefetch stages
     (4, 1, 34816, 5120, 1, dict(ctas=152, stages=3, prefetch_stages=2, smem_bytes=112640, consumer=0)),
-    # down 17408 -> 5120: ring at 1024 + 34816 = 35840; 2 x 33792 + 35840 = 103424
-    (4, 1, 5120, 17408, 1, dict(ctas=152, stages=2, prefetch_stages=2, smem_bytes=103424, consumer=0)),
-    # LM head at four rows: ring at 1024 + 40960 = 41984; 2 stages: 109568
-    (4, 4, 152064, 5120, 1, dict(ctas=152, stages=2, prefetch_stages=1, smem_bytes=109568, consumer=0)),
+    # down 17408 -> 5120: ring at 1024 + 34816 = 35840; 3 x 33792 + 35840 = 137216
+    (4, 1, 5120, 17408, 1, dict(ctas=152, stages=3, prefetch_stages=2, smem_bytes=137216, consumer=0)),
+    # LM head at four rows: ring at 1024 + 40960 = 41984; 3 stages: 143360
+    (4, 4, 152064, 5120, 1, dict(ctas=152, stages=3, prefetch_stages=1, smem_bytes=143360, consumer=0)),
     # two rows take four stages where they fit: 21504 + 4 x 33792 = 156672
     (4, 2, 7168, 5120, 1, dict(ctas=152, stages=4, prefetch_stages=1, smem_bytes=156672, consumer=0)),
-    # five rows: MMA consumer; nothing fits 115712, so the largest ring within the device limit:
-    # 52224 + 4 x 33792 = 187392
+    # five rows: MMA consumer, four stages: 52224 + 4 x 33792 = 187392
     (4, 5, 7168, 5120, 1, dict(ctas=152, stages=4, prefetch_stages=1, smem_bytes=187392, consumer=1)),
     # int8 entry: reduction buffer before 5120 B of q: ring at 3072 + 5120 = 8192; 3 stages: 109568
     (4, 1, 7168, 5120, 0, dict(ctas=152, stages=3, prefetch_stages=1, smem_bytes=109568, consumer=0)),
-    # int6: stages of 50176 B: 11264 + 2 x 50176 = 111616
-    (6, 1, 7168, 5120, 1, dict(ctas=152, stages=2, prefetch_stages=1, smem_bytes=111616, consumer=0)),
+    # int6: stages of 50176 B: 11264 + 3 x 50176 = 161792
+    (6, 1, 7168, 5120, 1, dict(ctas=152, stages=3, prefetch_stages=1, smem_bytes=161792, consumer=0)),
+
     # one block in all: one CTA; reduction buffer outside the 256-byte activation area:
     # ring at 3072 + 256 -> 3328; 3 stages: 104704
     (4, 1, 128, 128, 1, dict(ctas=1, stages=3, prefetch_stages=1, smem_bytes=104704, consumer=0)),

@@ -120,12 +120,10 @@ int smem_bytes_for(int bits, int M, int K, bool fused, int stages) {
   return ring_offset(M, K, fused, choose_consumer(bits, M)) + stages * kStageBlocks * block_bytes(bits);
 }
 
-// Shared memory a launch's ring and activations may take by default.  The kernel runs one CTA
-// per SM (nine warps of 100 or more registers: the 16,384-register file of a sub-partition then
-// holds at most four, so a second CTA never fits), and the next launch's CTA takes over an SM as soon
-// as this launch's CTA there exits.  A ring deeper than this budget puts more of the next
-// launch's weights in the memory queues ahead of the running launch's activation and partial
-// reads: 27B step at M = 1 2.33 ms, 2.40-2.41 ms with four to seven stages everywhere.
+// Shared memory a launch's ring and activations may take when the tuning override runs two CTAs
+// per SM.  By default the kernel runs one CTA per SM (nine warps of 100 or more registers: the
+// 16,384-register file of a sub-partition then holds at most four, so a second CTA never fits),
+// and the next launch's CTA takes over an SM as soon as this launch's CTA there exits.
 static constexpr int kRingBudget = (233472 - 2 * 1024) / 2;
 
 LaunchConfig choose_config(int bits, int M, int N, int K, bool fused, bool resident_grid) {
@@ -150,16 +148,13 @@ LaunchConfig choose_config_for(int sms, int smem_max, int bits, int M, int N, in
     const int budget = cps == 1 ? smem_max : ring_budget;
     while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > budget) --stages;
   } else {
-    // up to four stages within the ring budget, else the largest ring that fits.  Two rows take
-    // four stages wherever they fit (within the budget their 2 M K byte activations leave some
-    // linears only two stages): 27B step at M = 2 2.722 ms against 2.760 ms.
-    const int budget = M == 2 ? smem_max : ring_budget;
-    stages = 4;
-    while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > budget) --stages;
-    if (stages < 2 && cps == 1) {
-      stages = 4;
-      while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > smem_max) --stages;
-    }
+    // three stages wherever they fit the device's shared memory (two rows, and five or more,
+    // four), else the largest ring that fits.  27B step: three stages everywhere against up to
+    // four within half the shared memory (which left the down projection and every M = 4 launch
+    // two): M = 1 2.222 -> 2.193 ms, M = 3 2.975 -> 2.920, M = 4 3.388 -> 3.362; at M = 2 three and
+    // four stages are even (2.534 ms) and two lose (2.616); four at M = 1 lose (2.241).
+    stages = (M == 2 || M >= 5) ? 4 : 3;
+    while (stages >= 2 && smem_bytes_for(bits, M, K, fused, stages) > smem_max) --stages;
   }
   if (stages < 2) return cfg;
   const int stage_bytes = kStageBlocks * block_bytes(bits);
@@ -384,7 +379,7 @@ struct NextHint {
   int bits, N, K, kb;
 };
 static thread_local NextHint t_next = {nullptr, 0, 0, 0, 0};
-static constexpr int kPrefetchNextKb = 48;  // default per-CTA prefetch of the next linear (27B step sweep: 32-64 best)
+static constexpr int kPrefetchNextKb = 64;  // default per-CTA prefetch of the next linear (27B step: 32 - 96 KiB swept)
 
 // Fill the next-linear prefetch fields of p from a hint (none if the hint is empty or its
 // partition does not fit the 32-bit math); the next launch is planned like this one.
