@@ -488,9 +488,9 @@ static __device__ __noinline__ void prefetch_next_linear(const GemvParams& p, ui
 // amax pass then guarantees that every x value has been read before any q byte is
 // written.  Longer rows are quantised in rounds, each read in
 // full before any thread of the round writes (the amax pass has read everything
-// before the first write, so skipped rounds need no reads).  Every vector is stored
-// as the fast route gives it; one warp vote afterwards sends the rare vectors with a
-// quotient near a tie through the exact route, which stores them again.
+// before the first write, so skipped rounds need no reads).  A row's codes come from the
+// division-free corrected quotient (quantise8_fast) when its scale allows it (row_fast),
+// else from the IEEE division (quantise8_exact); both give rne(fl(x / s)).
 constexpr int kRegVecs = 12;  // 8-value vectors per thread kept in registers
 
 // Row scale s = RN(amax / 127) and rc = RN(1 / s) for a bf16 amax held in an fp32, by the
