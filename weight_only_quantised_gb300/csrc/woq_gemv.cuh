@@ -860,28 +860,15 @@ __device__ __forceinline__ void rmsnorm_quantise_regs(uint8_t* act, int K, int q
   }
 }
 
-// SwiGLU of eight (gate, up) pairs at g, u -> eight bf16 h bits
-__device__ __forceinline__ uint4 swiglu8(const float* __restrict__ g, const float* __restrict__ u) {
-  const float4 g0 = __ldg(reinterpret_cast<const float4*>(g)), g1 = __ldg(reinterpret_cast<const float4*>(g + 4));
-  const float4 u0 = __ldg(reinterpret_cast<const float4*>(u)), u1 = __ldg(reinterpret_cast<const float4*>(u + 4));
-  const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-  const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    o[i] = pro::swiglu_bf16(gg[2 * i], uu[2 * i]) | (pro::swiglu_bf16(gg[2 * i + 1], uu[2 * i + 1]) << 16);
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // Fused SwiGLU prologue, split over the grid.  h = SwiGLU(gate, up) of the fp32 [M][2K]
 // rows at gu (see woq_prologue.cuh).  The quantisation needs the largest |h| of each whole
-// row, and a CTA reads the k ranges of its own blocks, which many CTAs share.  So every CTA
-// forms h once for one C-th of each row, stores it (bf16) in the workspace scratch rows,
-// folds its largest |h| into the row words with red.max (h >= 0 as bits orders like the
-// values; the result does not depend on the order) and counts itself in with a release
-// reduction; once all C CTAs have (every CTA of this grid is resident, the wait is bounded)
-// it reads the row maxima and the h of its own ranges and quantises them like a bf16
-// activation.  sync (workspace, zero between launches): [0] arrivals, [2] departures
+// row, and a CTA reads the k ranges of its own blocks, which many CTAs share.  So each CTA of
+// the first half of the grid forms h once for its part of each row, stores it (bf16) in the
+// workspace scratch rows, folds its largest |h| into the row words with red.max (|h| as bits
+// orders like the values; the result does not depend on the order) and counts itself in
+// with a release reduction; once all of them have (every CTA of this grid is resident, the
+// wait is bounded) every CTA reads the row maxima and the h of its own ranges and quantises
+// them like a bf16 activation.  sync (workspace, zero between launches): [0] arrivals, [2] departures
 // (CTAs that have read the maxima), [8 + m] row m's largest |h| bits; CTA 0 zeroes them at
 // the end of the launch (swiglu_sync_reset).
 template <int M>
@@ -930,22 +917,26 @@ __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs
   if (tid < M) s_max[tid] = 0u;
   dev::named_barrier_sync(kBarConsumers, kConsumers);
   if (tid == 0) WOQ_TRACE_EV2(60);
-  // this CTA's slice of every row, in 8-value vectors: h once, into the scratch rows
-  const int nv = K / 8;
-  const int v_lo = (int)((unsigned long long)cta * (unsigned)nv / C);
-  const int v_hi = (int)((unsigned long long)(cta + 1) * (unsigned)nv / C);
+  // This CTA's slice of every row: h once, into the scratch rows, one value per consumer
+  // thread and pass (a slice is a few hundred values, so every thread takes part and the
+  // exp / reciprocal chain runs once per value rather than eight times in a row).  Only the
+  // first half of the grid forms slices: CTAs are placed in index order, and the last ones
+  // often start only when the previous grid ends, so the row maxima do not wait for them.
+  const uint32_t Cw = (C + 1) / 2;  // CTAs that form a slice
+  const int n_lo = cta < Cw ? (int)((unsigned long long)cta * (unsigned)K / Cw) : 0;
+  const int n_hi = cta < Cw ? (int)((unsigned long long)(cta + 1) * (unsigned)K / Cw) : 0;
   uint32_t acc[M];
 #pragma unroll
-  for (int m = 0; m < M; ++m) acc[m] = 0u;
-  for (int v = v_lo + tid; v < v_hi; v += kConsumers) {
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-      const uint4 h = swiglu8(gu + (size_t)m * 2 * K + 8 * v, gu + (size_t)m * 2 * K + K + 8 * v);
-      *reinterpret_cast<uint4*>(hbuf + (size_t)m * K + 8 * v) = h;
-      acc[m] = absmax8(acc[m], h);
+  for (int m = 0; m < M; ++m) {
+    acc[m] = 0u;
+    for (int k = n_lo + tid; k < n_hi; k += kConsumers) {
+      const uint32_t h = pro::swiglu_bf16(__ldg(gu + (size_t)m * 2 * K + k), __ldg(gu + (size_t)m * 2 * K + K + k));
+      hbuf[(size_t)m * K + k] = (uint16_t)h;
+      acc[m] = dev::bf16x2_absmax(acc[m], h);
     }
   }
-  swiglu_grid_max<M>(sync, C, acc, tid, lane, s_scratch, s_ok, wait_ns, skip_arrival, launch_id);  // also publishes the slices
+  // also publishes the slices; only the CTAs that formed one count themselves in
+  swiglu_grid_max<M>(sync, Cw, acc, tid, lane, s_scratch, s_ok, wait_ns, skip_arrival || cta >= Cw, launch_id);
   if (!*s_ok) return 0;
   // h of the k ranges this CTA's blocks read, written by the CTAs that own those slices
   // (read through L2: this SM's L1 may hold an older launch's lines)
