@@ -587,19 +587,6 @@ __device__ __forceinline__ void row_scales(const float (&lmax)[M], int tid, int 
   }
 }
 
-// Row scales from row amax values given in shared memory (the split SwiGLU prologue): the
-// same scale and reciprocal as row_scales, and the same consumer barrier.
-template <int M>
-__device__ __forceinline__ void given_row_scales(const float* amax_in, int tid, float* s_as, float (&sc)[M],
-                                                 float (&rc)[M]) {
-  dev::named_barrier_sync(kBarConsumers, kConsumers);
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    scale_and_rcp(amax_in[m], sc[m], rc[m]);
-    if (tid == 0) s_as[m] = sc[m];
-  }
-}
-
 // Whether a row's codes come from quantise8_fast: its scale s = RN(amax / 127) is zero (an
 // all-zero row: rc = 0 gives u = 0, q = 0) or at least 2^-123, i.e. amax >= 2^-116.  Uniform
 // across the row, so a warp never diverges on it.
@@ -617,8 +604,7 @@ __device__ __forceinline__ uint2 quantise8(uint4 xv, dev::f32x2 rc2, dev::f32x2 
 template <int M, bool X_GLOBAL = false>
 __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, int klo1, int khi1, int klo2, int khi2,
                                                   int tid, int lane, int warp, float* s_scratch, float* s_as,
-                                                  int launch_id, const float* amax_in = nullptr,
-                                                  const uint16_t* xg = nullptr) {
+                                                  int launch_id, const uint16_t* xg = nullptr) {
   constexpr int kVPR = kRegVecs / M;  // vectors per row held in registers
   constexpr int kStride = kConsumers * 8;  // values per vector round of all threads
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(act);
@@ -635,22 +621,18 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
         else
           xv[m][j] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
       }
-    if (amax_in) {  // the row amax is given: only the barrier (every x value read before any q byte is written)
-      given_row_scales<M>(amax_in, tid, s_as, sc, rc);
-    } else {
-      float lmax[M];
+    float lmax[M];
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        uint32_t acc = 0;
+    for (int m = 0; m < M; ++m) {
+      uint32_t acc = 0;
 #pragma unroll
-        for (int j = 0; j < kVPR; ++j) {
-          if (kStride * j >= K) break;  // warp-uniform
-          acc = absmax8(acc, xv[m][j]);  // zeros beyond the row
-        }
-        lmax[m] = dev::bf16x2_absmax_to_float(acc);
+      for (int j = 0; j < kVPR; ++j) {
+        if (kStride * j >= K) break;  // warp-uniform
+        acc = absmax8(acc, xv[m][j]);  // zeros beyond the row
       }
-      row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
+      lmax[m] = dev::bf16x2_absmax_to_float(acc);
     }
+    row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);  // every x value was read before this barrier
     if (tid == 0) WOQ_TRACE_EV2(5);
     dev::f32x2 rc2[M], ns2[M];
     bool fast[M];
@@ -672,26 +654,22 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
     }
     return;
   }
-  // longer rows: amax pass (unless given), then rounds of 4 vectors per thread over each row
-  if (amax_in) {
-    given_row_scales<M>(amax_in, tid, s_as, sc, rc);
-  } else {
-    float lmax[M];
+  // longer rows: amax pass, then rounds of 4 vectors per thread over each row
+  float lmax[M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      uint32_t a[4] = {0u, 0u, 0u, 0u};
-      int k = 8 * tid;
-      for (; k + 3 * kStride < K; k += 4 * kStride) {
+  for (int m = 0; m < M; ++m) {
+    uint32_t a[4] = {0u, 0u, 0u, 0u};
+    int k = 8 * tid;
+    for (; k + 3 * kStride < K; k += 4 * kStride) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          a[u] = absmax8(a[u], *reinterpret_cast<const uint4*>(xs + m * K + k + u * kStride));
-      }
-      for (; k < K; k += kStride) a[0] = absmax8(a[0], *reinterpret_cast<const uint4*>(xs + m * K + k));
-      lmax[m] = dev::bf16x2_absmax_to_float(dev::bf16x2_absmax(dev::bf16x2_absmax(a[0], a[1]),
-                                                               dev::bf16x2_absmax(a[2], a[3])));
+      for (int u = 0; u < 4; ++u)
+        a[u] = absmax8(a[u], *reinterpret_cast<const uint4*>(xs + m * K + k + u * kStride));
     }
-    row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);
+    for (; k < K; k += kStride) a[0] = absmax8(a[0], *reinterpret_cast<const uint4*>(xs + m * K + k));
+    lmax[m] = dev::bf16x2_absmax_to_float(dev::bf16x2_absmax(dev::bf16x2_absmax(a[0], a[1]),
+                                                             dev::bf16x2_absmax(a[2], a[3])));
   }
+  row_scales<M>(lmax, tid, lane, warp, s_scratch, s_as, sc, rc);
   if (tid == 0) WOQ_TRACE_EV2(5);
 #pragma unroll
   for (int m = 0; m < M; ++m) {
@@ -889,11 +867,12 @@ __device__ __forceinline__ void swiglu_grid_max(uint32_t* sync, uint32_t C, cons
     if (!skip_arrival) dev::red_add_release_u32(sync, 1u);  // ordered after the maxima
     bool ok = true;
     const uint64_t t0 = dev::global_timer_ns();
-    while (dev::ld_acquire_u32(sync) < C) {
+    while (dev::ld_acquire_u32(sync) < C) {  // one poller per CTA, backed off so the arrivals get through
       if (dev::global_timer_ns() - t0 > wait_ns) {
         ok = false;
         break;
       }
+      __nanosleep(32);
     }
     for (int m = 0; m < M; ++m) s_scratch[8 + m] = __uint_as_float(ok ? dev::ld_acquire_u32(sync + 8 + m) : 0u);
     if (ok) dev::red_add_release_u32(sync + 2, 1u);  // after the reads above
@@ -903,25 +882,22 @@ __device__ __forceinline__ void swiglu_grid_max(uint32_t* sync, uint32_t C, cons
   dev::named_barrier_sync(kBarConsumers, kConsumers);
 }
 
-// Returns 0 if the wait ran out, 1 if q is formed (register route), 2 if h is in the
-// activation area and the caller quantises it with the row maxima at s_scratch + 8.
+// Returns 0 if the wait ran out, 1 once q of this CTA's k ranges is in the activation area.
 template <int M>
 __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs, const float* __restrict__ gu,
                                                      uint32_t* sync, uint16_t* hbuf, uint32_t cta, uint32_t C,
                                                      int klo1, int khi1, int klo2, int khi2, int tid, int lane,
                                                      int warp, float* s_scratch, float* s_as, volatile int* s_ok,
                                                      uint64_t wait_ns, bool skip_arrival, int launch_id) {
-  constexpr int kStride = kConsumers * 8;
-  constexpr int kHV = M <= 4 ? 4 / M : 1;  // vectors per row and range kept in registers
   uint32_t* s_max = reinterpret_cast<uint32_t*>(s_scratch);
   if (tid < M) s_max[tid] = 0u;
   dev::named_barrier_sync(kBarConsumers, kConsumers);
   if (tid == 0) WOQ_TRACE_EV2(60);
   // This CTA's slice of every row: h once, into the scratch rows, one value per consumer
   // thread and pass (a slice is a few hundred values, so every thread takes part and the
-  // exp / reciprocal chain runs once per value rather than eight times in a row).  Only the
-  // first half of the grid forms slices: CTAs are placed in index order, and the last ones
-  // often start only when the previous grid ends, so the row maxima do not wait for them.
+  // exp / reciprocal chain runs once per value rather than eight times in a row).  Only the first half of the
+  // grid forms slices: CTAs are placed in index order, and the last ones often start only
+  // when the previous grid ends, so the row maxima do not wait for them.
   const uint32_t Cw = (C + 1) / 2;  // CTAs that form a slice
   const int n_lo = cta < Cw ? (int)((unsigned long long)cta * (unsigned)K / Cw) : 0;
   const int n_hi = cta < Cw ? (int)((unsigned long long)(cta + 1) * (unsigned)K / Cw) : 0;
@@ -938,55 +914,52 @@ __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs
   // also publishes the slices; only the CTAs that formed one count themselves in
   swiglu_grid_max<M>(sync, Cw, acc, tid, lane, s_scratch, s_ok, wait_ns, skip_arrival || cta >= Cw, launch_id);
   if (!*s_ok) return 0;
-  // h of the k ranges this CTA's blocks read, written by the CTAs that own those slices
-  // (read through L2: this SM's L1 may hold an older launch's lines)
-  if (khi1 - klo1 <= kHV * kStride && khi2 - klo2 <= kHV * kStride) {  // register route (CTA-uniform)
-    uint4 hv[2][kHV][M];
+  float sc[M];
+  dev::f32x2 rc2[M], ns2[M];
+  bool fast[M];
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int j = 0; j < kHV; ++j) {
-        const int k = (r == 0 ? klo1 : klo2) + 8 * tid + j * kStride;
-        if (k < (r == 0 ? khi1 : khi2)) {
-#pragma unroll
-          for (int m = 0; m < M; ++m) hv[r][j][m] = __ldcg(reinterpret_cast<const uint4*>(hbuf + (size_t)m * K + k));
-        }
-      }
-    float sc[M], rc[M];
-    dev::f32x2 rc2[M], ns2[M];
-    bool fast[M];
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-      scale_and_rcp(s_scratch[8 + m], sc[m], rc[m]);
-      rc2[m] = dev::f2_splat(rc[m]);
-      ns2[m] = dev::f2_splat(-sc[m]);
-      fast[m] = row_fast(sc[m]);
-    }
-    if (tid < M) s_as[tid] = sc[tid];
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int j = 0; j < kHV; ++j) {
-        const int k = (r == 0 ? klo1 : klo2) + 8 * tid + j * kStride;
-        if (k < (r == 0 ? khi1 : khi2)) {
-#pragma unroll
-          for (int m = 0; m < M; ++m)
-            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(hv[r][j][m], rc2[m], ns2[m], sc[m], fast[m]);
-        }
-      }
-    return 1;
+  for (int m = 0; m < M; ++m) {
+    float rc;
+    scale_and_rcp(s_scratch[8 + m], sc[m], rc);
+    rc2[m] = dev::f2_splat(rc);
+    ns2[m] = dev::f2_splat(-sc[m]);
+    fast[m] = row_fast(sc[m]);
   }
-  // shared-memory route: h (bf16) of the ranges into the activation area
-  uint16_t* hs = reinterpret_cast<uint16_t*>(act);
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int lo = r == 0 ? klo1 : klo2, hi = r == 0 ? khi1 : khi2;
+  for (int m = 0; m < M; ++m)
+    if (tid == m) s_as[m] = sc[m];
+  // h of the k ranges this CTA's blocks read, written by the CTAs that own those slices,
+  // read through L2 (this SM's L1 may hold an older launch's lines) and quantised straight
+  // into the activation area: per batch up to kHB vectors of 8 values per row and thread,
+  // every load issued before the first is used, so a batch costs one round trip (one batch
+  // covers the 27B down projection's ranges at M <= 4)
+  constexpr int kHB = M <= 2 ? 4 : (M <= 4 ? 3 : 1);
+  const int nv1 = (khi1 - klo1) / 8, nv2 = (khi2 - klo2) / 8;
+  const int per_row = nv1 + nv2;
+  for (int v0 = tid; v0 < per_row; v0 += kHB * kConsumers) {
+    uint4 hv[M][kHB];
 #pragma unroll
     for (int m = 0; m < M; ++m)
-      for (int k = lo + 8 * tid; k < hi; k += kStride)
-        *reinterpret_cast<uint4*>(hs + m * K + k) = __ldcg(reinterpret_cast<const uint4*>(hbuf + (size_t)m * K + k));
+#pragma unroll
+      for (int b = 0; b < kHB; ++b) {
+        const int v = v0 + b * kConsumers;
+        if (v < per_row) {
+          const int k = v < nv1 ? klo1 + 8 * v : klo2 + 8 * (v - nv1);
+          hv[m][b] = __ldcg(reinterpret_cast<const uint4*>(hbuf + (size_t)m * K + k));
+        }
+      }
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+      for (int b = 0; b < kHB; ++b) {
+        const int v = v0 + b * kConsumers;
+        if (v < per_row) {
+          const int k = v < nv1 ? klo1 + 8 * v : klo2 + 8 * (v - nv1);
+          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(hv[m][b], rc2[m], ns2[m], sc[m], fast[m]);
+        }
+      }
   }
-  return 2;
+  return 1;
 }
 
 // End of a launch with the split SwiGLU prologue: CTA 0 waits (bounded) until every CTA
@@ -1250,9 +1223,6 @@ __global__ void __maxnreg__(168) gemv_kernel(const GemvParams p) {
                                                p.hbuf, cta, C, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch,
                                                s_as, s_flags + 3, p.wait_ns, p.fault == 2 && cta == p.fault_cta,
                                                p.launch_id);
-    if (route == 2)
-      quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
-                           p.launch_id, s_scratch + 8);
     if (tid == 0) WOQ_TRACE_EV(63);
     if (route == 0) {
       aborted = true;
@@ -1264,7 +1234,7 @@ __global__ void __maxnreg__(168) gemv_kernel(const GemvParams p) {
   } else if constexpr (PRO == kProBf16) {
     if (kXDirect && x_direct)
       quantise_prologue<M, kXDirect>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
-                                 p.launch_id, nullptr, static_cast<const uint16_t*>(p.x));
+                                 p.launch_id, static_cast<const uint16_t*>(p.x));
     else
       quantise_prologue<M>(act, p.K, p.act_stride, klo1, khi1, klo2, khi2, tid, lane, warp, s_scratch, s_as,
                            p.launch_id);
