@@ -642,14 +642,30 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
       ns2[m] = dev::f2_splat(-sc[m]);
       fast[m] = row_fast(sc[m]);
     }
+    bool all_fast = true;  // CTA-uniform: the division route's call stays out of the common loop
 #pragma unroll
-    for (int j = 0; j < kVPR; ++j) {
-      if (kStride * j >= K) break;  // uniform
-      const int k = 8 * tid + kStride * j;
-      if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {  // read by this CTA
+    for (int m = 0; m < M; ++m) all_fast = all_fast && fast[m];
+    if (all_fast) {
 #pragma unroll
-        for (int m = 0; m < M; ++m)
-          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(xv[m][j], rc2[m], ns2[m], sc[m], fast[m]);
+      for (int j = 0; j < kVPR; ++j) {
+        if (kStride * j >= K) break;  // uniform
+        const int k = 8 * tid + kStride * j;
+        if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {  // read by this CTA
+#pragma unroll
+          for (int m = 0; m < M; ++m)
+            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(xv[m][j], rc2[m], ns2[m]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kVPR; ++j) {
+        if (kStride * j >= K) break;  // uniform
+        const int k = 8 * tid + kStride * j;
+        if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2))) {
+#pragma unroll
+          for (int m = 0; m < M; ++m)
+            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(xv[m][j], rc2[m], ns2[m], sc[m], fast[m]);
+        }
       }
     }
     return;
@@ -675,7 +691,7 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
   for (int m = 0; m < M; ++m) {
     const dev::f32x2 rc2 = dev::f2_splat(rc[m]);
     const dev::f32x2 ns2 = dev::f2_splat(-sc[m]);
-    const bool fast = row_fast(sc[m]);
+    const bool fast = row_fast(sc[m]);  // CTA-uniform: the division route's call stays out of the common loop
     for (int k0 = 0; k0 < K; k0 += 4 * kStride) {
       // CTA-uniform: skip rounds that hold no k this CTA reads
       if (!((k0 < khi1 && k0 + 4 * kStride > klo1) || (k0 < khi2 && k0 + 4 * kStride > klo2))) continue;
@@ -686,11 +702,20 @@ __device__ __forceinline__ void quantise_prologue(uint8_t* act, int K, int qs, i
         xv[v] = k < K ? *reinterpret_cast<const uint4*>(xs + m * K + k) : make_uint4(0, 0, 0, 0);
       }
       dev::named_barrier_sync(kBarConsumers, kConsumers);
+      if (fast) {
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int k = k0 + 8 * tid + kStride * v;
-        if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2)))
-          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(xv[v], rc2, ns2, sc[m], fast);
+        for (int v = 0; v < 4; ++v) {
+          const int k = k0 + 8 * tid + kStride * v;
+          if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2)))
+            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(xv[v], rc2, ns2);
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int k = k0 + 8 * tid + kStride * v;
+          if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2)))
+            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_exact(xv[v], sc[m]);
+        }
       }
     }
   }
@@ -828,12 +853,20 @@ __device__ __forceinline__ void rmsnorm_quantise_regs(uint8_t* act, int K, int q
     if (tid == 0) s_as[m] = sc;
     const dev::f32x2 rc2 = dev::f2_splat(rc);
     const dev::f32x2 ns2 = dev::f2_splat(-sc);
-    const bool fast = row_fast(sc);
+    if (row_fast(sc)) {  // CTA-uniform: the division route's call stays out of the common loop
 #pragma unroll
-    for (int j = 0; j < kRmsRegVecs; ++j) {
-      const int k = 8 * tid + kStride * j;
-      if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2)))
-        *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(v[m][j], rc2, ns2, sc, fast);
+      for (int j = 0; j < kRmsRegVecs; ++j) {
+        const int k = 8 * tid + kStride * j;
+        if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2)))
+          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(v[m][j], rc2, ns2);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kRmsRegVecs; ++j) {
+        const int k = 8 * tid + kStride * j;
+        if (k < K && ((k >= klo1 && k < khi1) || (k >= klo2 && k < khi2)))
+          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_exact(v[m][j], sc);
+      }
     }
   }
 }
@@ -949,15 +982,27 @@ __device__ __forceinline__ int swiglu_split_prologue(uint8_t* act, int K, int qs
         }
       }
 #pragma unroll
-    for (int m = 0; m < M; ++m)
+    for (int m = 0; m < M; ++m) {
+      if (fast[m]) {  // CTA-uniform: the division route's call stays out of the common loop
 #pragma unroll
-      for (int b = 0; b < kHB; ++b) {
-        const int v = v0 + b * kConsumers;
-        if (v < per_row) {
-          const int k = v < nv1 ? klo1 + 8 * v : klo2 + 8 * (v - nv1);
-          *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8(hv[m][b], rc2[m], ns2[m], sc[m], fast[m]);
+        for (int b = 0; b < kHB; ++b) {
+          const int v = v0 + b * kConsumers;
+          if (v < per_row) {
+            const int k = v < nv1 ? klo1 + 8 * v : klo2 + 8 * (v - nv1);
+            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_fast(hv[m][b], rc2[m], ns2[m]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int b = 0; b < kHB; ++b) {
+          const int v = v0 + b * kConsumers;
+          if (v < per_row) {
+            const int k = v < nv1 ? klo1 + 8 * v : klo2 + 8 * (v - nv1);
+            *reinterpret_cast<uint2*>(act + m * qs + k) = quantise8_exact(hv[m][b], sc[m]);
+          }
         }
       }
+    }
   }
   return 1;
 }
