@@ -1450,7 +1450,7 @@ __global__ void __maxnreg__(168) gemv_kernel(const GemvParams p) {
                   const uint64_t t0 = dev::global_timer_ns();
                   while (!(v >> 32)) {
                     if (dev::global_timer_ns() - t0 > p.wait_ns) break;
-                    __nanosleep(64);
+                    __nanosleep(16);
                     v = dev::ld_relaxed_u64(src[b] + m * kTileRows);
                   }
                 }
