@@ -349,16 +349,16 @@ typedef struct {
 } woq_launch_plan;
 WOQ_API int woq_plan_launch(int bits, int M, int N, int K, int entry, int sms, int smem_max, woq_launch_plan* out);
 
-/* Tests of the bounded waits (section 8(b) of no page: the pages describe no failure
- * handling; every wait of a woq kernel on another CTA is bounded so that a stuck CTA
- * never hangs a shared GPU).  Injects one fault into the following launches of this
+/* Tests of the bounded waits (the pages describe no failure handling; every wait of a woq
+ * kernel on another CTA is bounded so that a stuck CTA never hangs a shared GPU).  Injects one fault into the following launches of this
  * process, made by CTA `cta` (a block index), and bounds the waits it makes run out by
  * wait_limit_us microseconds (0 = the default, 2 s):
  *   kind 1: GEMV / linear launches - that CTA never publishes its split-tile partial
  *           sums; the combiner of such a tile gives up, sets WOQ_DEVERR_TIMEOUT and
  *           leaves that tile's rows of y untouched;
- *   kind 2: SwiGLU linears - that CTA never counts itself in at the row maxima; every
- *           CTA gives up, sets WOQ_DEVERR_TIMEOUT and leaves y untouched;
+ *   kind 2: SwiGLU linears - that CTA (one of the first half of the grid, the CTAs that
+ *           form the row maxima) never counts itself in; every CTA gives up, sets
+ *           WOQ_DEVERR_TIMEOUT and leaves y untouched;
  *   kind 3: woq_relayout_inplace - that CTA leaves before the first grid barrier; the
  *           others give up and the call returns WOQ_ERR_DEVICE (buffer contents undefined);
  *   kind 0: no fault (the default).
